@@ -1,0 +1,243 @@
+/*
+ * Plain CPU oracle for the memory-bound MoE glue path:
+ * routing (softmax, top-k, optional renormalisation), the expert-sorted
+ * permutation (histogram, exclusive scan, stable counting sort), row
+ * expansion, the SwiGLU activation and the weighted top-k combine.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or
+ * call this file: only the tests, the package smoke check and the benchmark's
+ * CPU-baseline leg use it. It shares no code, header, table or constant with
+ * the CUDA library.
+ *
+ * Sources (page title, then section):
+ *  - "CuTeDSL at Perplexity", section "Mixture of Experts (MoE) dispatch/combine",
+ *    sub-section "Local": the local kernel counts the tokens routed to each
+ *    expert, gives every token a unique index inside its expert's list, copies
+ *    the tokens into a buffer for the expert GEMM, and the combine kernel uses
+ *    those token positions to accumulate the expert outputs into the final
+ *    token.
+ *  - "[FlashInfer] CUTLASS MoE kernel optimisation" (flashinfer PR #3761
+ *    analysis), section 1 "Explicit vectorization" and section 2 "Dynamic
+ *    threads": expandInputRows copies rows into expert order; doActivation
+ *    applies the gated activation (SwiGLU for Qwen3) to the fc1 output.
+ *  The pages give no formulas for softmax, top-k, SwiGLU or combine; the
+ *  plain textbook definitions are used, with these readings:
+ *   - top-k selects on the logits (order-equivalent to the softmax
+ *     probabilities), larger first, equal logits -> lower expert index first;
+ *     -0.0 and +0.0 compare equal;
+ *   - softmax runs over all E experts; renormalisation divides each selected
+ *     probability by the sum of the k selected ones;
+ *   - the permutation is stable in the flat slot s = t*k + j;
+ *   - gate occupies columns [0, I) of the fc1 row and up occupies [I, 2I);
+ *     act = silu(gate) * up with silu(g) = g / (1 + exp(-g));
+ *   - combine sums w[t,j] * expert_out[inv_perm[t*k+j], :] over j.
+ *
+ * Precision: every real-valued quantity is computed in IEEE double and
+ * rounded ONCE to the output type (float for routing weights, bfloat16 with
+ * round-to-nearest-even for activations). bfloat16 values are passed as their
+ * 16-bit patterns (uint16_t).
+ *
+ * Build: cc -std=c11 -O2 -ffp-contract=off -fPIC -shared moe_oracle.c -lm
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------------- */
+/* bfloat16 <-> real                                                       */
+/* ---------------------------------------------------------------------- */
+
+/* bfloat16 is the top half of an IEEE binary32: decoding is exact. */
+static double bf16_to_double(uint16_t h) {
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Round a real number once to bfloat16, round-to-nearest, ties to even.
+ * bfloat16 has binary32's exponent range (normal exponents -126..127,
+ * subnormals below) and 7 stored fraction bits, so the spacing of
+ * representable values around |v| in [2^e, 2^(e+1)) is 2^(max(e,-126)-7).
+ * v / spacing is exact (power-of-two scaling) and rint() rounds it half to
+ * even under the default rounding mode. Results of 2^128 or more overflow. */
+static uint16_t bf16_round(double v) {
+    if (isnan(v)) return (uint16_t)0x7FC0u;
+    uint16_t sign = signbit(v) ? (uint16_t)0x8000u : (uint16_t)0u;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+    int e2;
+    (void)frexp(a, &e2); /* a = f * 2^e2, f in [0.5, 1): leading bit is 2^(e2-1) */
+    int lead = e2 - 1;
+    if (lead < -126) lead = -126;
+    double spacing = ldexp(1.0, lead - 7);
+    double r = rint(a / spacing) * spacing;
+    if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80u);
+    float f = (float)r; /* exact: at most 8 significant bits, in range */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(sign | (uint16_t)(bits >> 16));
+}
+
+/* Exposed so the tests can pin the rounding against known values. */
+void oracle_bf16_round(const double* in, long n, uint16_t* out) {
+    for (long i = 0; i < n; ++i) out[i] = bf16_round(in[i]);
+}
+
+void oracle_bf16_decode(const uint16_t* in, long n, double* out) {
+    for (long i = 0; i < n; ++i) out[i] = bf16_to_double(in[i]);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Routing: softmax + top-k + optional renormalisation                     */
+/* ---------------------------------------------------------------------- */
+
+/* For each token t (row of logits[T][E]):
+ *   p_e = exp(l_e - max l) / sum_e' exp(l_e' - max l)          (softmax, all E)
+ *   ids = the k experts with the largest logits, in descending order of
+ *         logit; equal logits are taken lower index first
+ *   w_j = p_{ids_j}                              (renorm == 0)
+ *   w_j = p_{ids_j} / sum_{j'} p_{ids_j'}        (renorm != 0)
+ * Returns 0, or -1 on bad sizes or allocation failure. */
+int oracle_route_topk(const float* logits, long T, int E, int k, int renorm,
+                      int32_t* topk_ids, float* topk_weights) {
+    if (T < 0 || E < 1 || k < 1 || k > E) return -1;
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    if (!p || !taken) { free(p); free(taken); return -1; }
+    for (long t = 0; t < T; ++t) {
+        const float* l = logits + t * (long)E;
+        double m = (double)l[0];
+        for (int e = 1; e < E; ++e)
+            if ((double)l[e] > m) m = (double)l[e];
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) {
+            p[e] = exp((double)l[e] - m);
+            z += p[e];
+        }
+        for (int e = 0; e < E; ++e) p[e] /= z;
+
+        memset(taken, 0, (size_t)E);
+        double sel_sum = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                /* strictly greater: on equal logits the lower index stays */
+                if (best < 0 || l[e] > l[best]) best = e;
+            }
+            taken[best] = 1;
+            topk_ids[t * k + j] = (int32_t)best;
+            sel_sum += p[best];
+        }
+        for (int j = 0; j < k; ++j) {
+            double w = p[topk_ids[t * k + j]];
+            if (renorm) w /= sel_sum;
+            topk_weights[t * k + j] = (float)w;
+        }
+    }
+    free(p);
+    free(taken);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Permutation: histogram, exclusive scan, stable counting sort            */
+/* ---------------------------------------------------------------------- */
+
+/* Slots s = t*k + j, S = T*k, expert e_s = topk_ids[s].
+ *   counts[e]    = #{ s : e_s = e }
+ *   offsets[e]   = sum_{e' < e} counts[e'],  offsets[E] = S
+ *   p(s)         = offsets[e_s] + #{ s' < s : e_s' = e_s }
+ *   perm[p(s)]   = s,  inv_perm[s] = p(s)
+ * Returns 0, or -1 if an id lies outside [0, E). */
+int oracle_route_permute(const int32_t* topk_ids, long T, int E, int k,
+                         int32_t* counts, int32_t* offsets,
+                         int32_t* perm, int32_t* inv_perm) {
+    long S = T * (long)k;
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (long s = 0; s < S; ++s) {
+        int32_t e = topk_ids[s];
+        if (e < 0 || e >= E) return -1;
+        counts[e] += 1;
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int32_t* next = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
+    if (!next) return -1;
+    for (int e = 0; e < E; ++e) next[e] = offsets[e];
+    for (long s = 0; s < S; ++s) {
+        int32_t e = topk_ids[s];
+        int32_t pos = next[e]++;
+        perm[pos] = (int32_t)s;
+        inv_perm[s] = pos;
+    }
+    free(next);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Expand: expert-sorted copy of token rows                                */
+/* ---------------------------------------------------------------------- */
+
+/* expanded_x[p, :] = x[perm[p] / k, :] for p in [0, P). Bit copy.
+ * P may be smaller than T*k to produce a contiguous block of rows
+ * (pass perm + p0). Returns -1 if a source token falls outside [0, T). */
+int oracle_expand(const uint16_t* x, long T, int H, int k,
+                  const int32_t* perm, long P, uint16_t* expanded_x) {
+    for (long p = 0; p < P; ++p) {
+        long t = (long)perm[p] / k;
+        if (perm[p] < 0 || t >= T) return -1;
+        memcpy(expanded_x + p * (long)H, x + t * (long)H, sizeof(uint16_t) * (size_t)H);
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* SwiGLU                                                                  */
+/* ---------------------------------------------------------------------- */
+
+/* act[r, i] = bf16( silu(g) * u ), g = gate_up[r, i], u = gate_up[r, I + i],
+ * silu(g) = g / (1 + exp(-g)); real arithmetic, one rounding. */
+void oracle_swiglu(const uint16_t* gate_up, long rows, int I, uint16_t* act) {
+    for (long r = 0; r < rows; ++r) {
+        const uint16_t* gate = gate_up + r * 2L * I;
+        const uint16_t* up = gate + I;
+        for (int i = 0; i < I; ++i) {
+            double g = bf16_to_double(gate[i]);
+            double u = bf16_to_double(up[i]);
+            double silu = g / (1.0 + exp(-g));
+            act[r * (long)I + i] = bf16_round(silu * u);
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Combine: weighted sum of each token's k expert rows                     */
+/* ---------------------------------------------------------------------- */
+
+/* out[t, :] = bf16( sum_{j<k} w[t, j] * expert_out[inv_perm[t*k + j], :] ),
+ * summed in real arithmetic for j = 0..k-1 and rounded once.
+ * S is the number of rows of expert_out (for the range check); T may be a
+ * sub-range of tokens if w and inv_perm are offset to match.
+ * Returns -1 if a row index falls outside [0, S). */
+int oracle_combine(const uint16_t* expert_out, long S, int H, int k, long T,
+                   const float* w, const int32_t* inv_perm, uint16_t* out) {
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!acc) return -1;
+    for (long t = 0; t < T; ++t) {
+        for (int c = 0; c < H; ++c) acc[c] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            long p = inv_perm[t * k + j];
+            if (p < 0 || p >= S) { free(acc); return -1; }
+            double wj = (double)w[t * k + j];
+            const uint16_t* row = expert_out + p * (long)H;
+            for (int c = 0; c < H; ++c) acc[c] += wj * bf16_to_double(row[c]);
+        }
+        for (int c = 0; c < H; ++c) out[t * (long)H + c] = bf16_round(acc[c]);
+    }
+    free(acc);
+    return 0;
+}
