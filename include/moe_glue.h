@@ -1,0 +1,183 @@
+/*
+ * moe_glue.h - C ABI of the GB300 (sm_103a) memory-bound MoE glue path.
+ *
+ * One MoE layer calls, in order:
+ *   moe_route   router logits -> top-k experts, weights, per-expert counts and
+ *               offsets, and the expert-sorted permutation
+ *   moe_expand  token rows -> expert-sorted rows (input of the fc1 GEMM)
+ *   moe_swiglu  fc1 output [gate | up] -> silu(gate) * up (input of fc2)
+ *   moe_combine fc2 output rows -> weighted sum of each token's k rows
+ * The expert GEMMs between these calls are not part of this library.
+ *
+ * Conventions shared by every entry point
+ *   - T tokens, E experts, k experts per token, S = T*k (token, expert) slots.
+ *     The flat slot index is s = t*k + j for the j-th expert of token t; the
+ *     expert-sorted row index is p.
+ *   - bfloat16 tensors are passed as moe_bf16_t (the 16-bit pattern), all
+ *     matrices are dense row-major with no padding between rows.
+ *   - Every pointer is a DEVICE pointer of the current CUDA device (or
+ *     managed memory), allocated and owned by the caller. The library never
+ *     allocates, frees or keeps a pointer after the call returns.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns before it runs. MOE_OK means "validated and
+ *     launched"; a device-side fault surfaces at the caller's next
+ *     synchronisation.
+ *   - Arguments are validated on the host before anything is launched: on any
+ *     error status other than MOE_ERR_CUDA nothing has been enqueued and no
+ *     output has been written. MOE_ERR_CUDA reports a failed launch; outputs
+ *     are then unspecified.
+ *   - Inputs are read-only. Outputs must not overlap any input or each other
+ *     (checked from the address ranges; MOE_ERR_INVALID_ARG).
+ *   - bfloat16 matrices and the routing workspace must be 16-byte aligned
+ *     and every bfloat16 row must be a whole number of 16-byte vectors, i.e.
+ *     its width a multiple of 8 elements (MOE_ERR_MISALIGNED): the 128-bit
+ *     access rule of the "[FlashInfer] CUTLASS MoE kernel optimisation"
+ *     analysis (flashinfer PR #3761), section 3 "Strict memory alignment
+ *     validation". int32 and float32 arrays need their natural 4-byte
+ *     alignment.
+ *   - A zero-sized batch (T = 0 or rows = 0) is valid; pointers of empty
+ *     arrays may then be NULL.
+ *   - The functions are thread-safe and keep no mutable global state apart
+ *     from a per-device cache of the SM count.
+ *
+ * Page citations name the page title and section; the pages themselves
+ * state no formulas, so the definitions below are the plain readings
+ * (softmax over all experts, top-k on logits with the lower index first on
+ * ties, renormalisation over the k chosen, stable expert order, gate in the
+ * first half of the fc1 row).
+ */
+#ifndef MOE_GLUE_H
+#define MOE_GLUE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Identical to cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st* moe_stream_t;
+
+/* A bfloat16 value as its IEEE bit pattern (sign, 8 exponent, 7 fraction bits). */
+typedef uint16_t moe_bf16_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* negative size, k < 1, k > E, NULL pointer, overlapping buffers */
+    MOE_ERR_MISALIGNED = 2,   /* pointer not 16-byte aligned or row not a multiple of 16 bytes */
+    MOE_ERR_UNSUPPORTED = 3,  /* E > MOE_MAX_EXPERTS, k > MOE_MAX_TOPK, T*k >= 2^31 */
+    MOE_ERR_WORKSPACE = 4,    /* workspace smaller than moe_route_workspace_size() */
+    MOE_ERR_CUDA = 5          /* a CUDA launch failed (see cudaGetLastError semantics) */
+} moe_status_t;
+
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 16
+
+/* Human-readable name of a status code. Never NULL; static storage. */
+const char* moe_status_string(moe_status_t status);
+
+/*
+ * Bytes of device workspace moe_route needs for (T, E, k); 0 when the
+ * single-block path applies (small T). A pure function of its arguments.
+ * Errors: MOE_ERR_INVALID_ARG (bytes NULL, T < 0, E < 1, k < 1, k > E),
+ * MOE_ERR_UNSUPPORTED (E > MOE_MAX_EXPERTS, k > MOE_MAX_TOPK, T*k >= 2^31).
+ */
+moe_status_t moe_route_workspace_size(int64_t T, int E, int k, size_t* bytes);
+
+/*
+ * Top-k routing and the expert-sorted permutation.
+ * "CuTeDSL at Perplexity", section "Mixture of Experts (MoE) dispatch/combine",
+ * sub-section "Local": from the routing table, count the tokens assigned to
+ * each expert and give every token a unique index inside its expert's list;
+ * the prefill variant counts per block and aggregates the counts of all
+ * blocks in global memory to place each token.
+ *
+ * For each token t, with l = logits[t, 0..E-1] (float32, row-major [T, E]):
+ *   softmax   p_e = exp(l_e - max l) / sum_e' exp(l_e' - max l), over all E
+ *   top-k     topk_ids[t, 0..k-1] = the k experts with the largest logits in
+ *             descending order; equal logits (-0.0 == +0.0) go lower index
+ *             first. Selection compares the float32 logits, so it is exact.
+ *   weights   topk_weights[t, j] = p_{id_j}                      (renorm == 0)
+ *                                = p_{id_j} / sum_j' p_{id_j'}   (renorm != 0)
+ *             computed in float32.
+ * Over the S = T*k slots s = t*k + j with expert e_s = topk_ids[s]:
+ *   expert_counts[e]  = #{ s : e_s = e }                            [E]
+ *   expert_offsets[e] = sum_{e' < e} expert_counts[e'];
+ *   expert_offsets[E] = S                                           [E + 1]
+ *   inv_perm[s] = p   = expert_offsets[e_s] + #{ s' < s : e_s' = e_s }   [S]
+ *   perm[p]     = s                                                      [S]
+ * The permutation is deterministic (stable in s): bit-identical run to run.
+ *
+ * Outputs topk_ids [T, k] int32, topk_weights [T, k] float32, expert_counts,
+ * expert_offsets, perm and inv_perm (int32) are written in full.
+ * workspace: device scratch of at least moe_route_workspace_size(T, E, k)
+ * bytes, 16-byte aligned (may be NULL when that size is 0); its contents on
+ * entry are ignored and on return are unspecified. Calls that share a
+ * workspace must be ordered (same stream or synchronised).
+ * Logits are assumed finite; NaN logits give unspecified (but in-bounds)
+ * results. T = 0 writes zero counts and offsets.
+ */
+moe_status_t moe_route(const float* logits, int64_t T, int E, int k, int renorm,
+                       int32_t* topk_ids, float* topk_weights,
+                       int32_t* expert_counts, int32_t* expert_offsets,
+                       int32_t* perm, int32_t* inv_perm,
+                       void* workspace, size_t workspace_bytes,
+                       moe_stream_t stream);
+
+/*
+ * Row expansion into expert order (expandInputRows).
+ * "CuTeDSL at Perplexity", section "Mixture of Experts (MoE) dispatch/combine",
+ * sub-section "Local" (tokens are copied to the buffer the MoE GEMM reads),
+ * and "[FlashInfer] CUTLASS MoE kernel optimisation", section 1 "Explicit
+ * vectorization" (expandInputRowsKernel, 128-bit loads and stores).
+ *
+ *   expanded_x[inv_perm[t*k + j], :] = x[t, :]   for all t < T, j < k
+ * i.e. expanded_x[p, :] = x[perm[p] / k, :]: a bit copy of bfloat16 rows.
+ * x [T, H], inv_perm [T*k] (a permutation of 0..S-1, as moe_route writes
+ * it), expanded_x [S, H]. H must be a multiple of 8. Entries of inv_perm
+ * outside [0, S) are skipped (their rows are not written); if inv_perm is not
+ * a permutation some rows stay unwritten.
+ */
+moe_status_t moe_expand(const moe_bf16_t* x, int64_t T, int H, int k,
+                        const int32_t* inv_perm, moe_bf16_t* expanded_x,
+                        moe_stream_t stream);
+
+/*
+ * Gated SwiGLU activation (doActivation).
+ * "[FlashInfer] CUTLASS MoE kernel optimisation", section 1 "Explicit
+ * vectorization" and section 2 "Dynamic threads" (doActivationKernel over the
+ * fc1 output, block size chosen from the intermediate size).
+ *
+ *   act[r, i] = bf16_rn( silu(g) * u ),  g = gate_up[r, i], u = gate_up[r, I + i],
+ *   silu(g) = g / (1 + exp(-g)),  computed in float32, rounded once to
+ *   bfloat16 (nearest, ties to even).
+ * gate_up [rows, 2I] (gate = first I columns, up = last I), act [rows, I].
+ * I must be a multiple of 8.
+ */
+moe_status_t moe_swiglu(const moe_bf16_t* gate_up, int64_t rows, int I,
+                        moe_bf16_t* act, moe_stream_t stream);
+
+/*
+ * Weighted top-k combine / unpermute.
+ * "CuTeDSL at Perplexity", section "Mixture of Experts (MoE) dispatch/combine",
+ * sub-section "Local" (the combine kernel uses the token positions from the
+ * routing step, accumulates in registers and writes the final token) and the
+ * same section's note that combine is a vectorised accumulation.
+ *
+ *   out[t, :] = bf16_rn( sum_{j=0}^{k-1} topk_weights[t, j] *
+ *                        expert_out[inv_perm[t*k + j], :] )
+ * accumulated in float32 in order j = 0..k-1, rounded once.
+ * expert_out [S, H], topk_weights [T, k] float32, inv_perm [T*k], out [T, H].
+ * H must be a multiple of 8. Entries of inv_perm outside [0, S) contribute
+ * nothing.
+ */
+moe_status_t moe_combine(const moe_bf16_t* expert_out, int64_t T, int H, int k,
+                         const float* topk_weights, const int32_t* inv_perm,
+                         moe_bf16_t* out, moe_stream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* MOE_GLUE_H */

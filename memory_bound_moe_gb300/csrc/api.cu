@@ -1,0 +1,202 @@
+// C-ABI entry points (declared in include/moe_glue.h): argument validation on
+// the host, then one launch sequence on the caller's stream. No allocation,
+// no synchronisation, no host copies, no fallback path.
+#include "moe_glue.h"
+#include "moe_launch.h"
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+namespace {
+
+using moe::RoutePlan;
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+// SM count of the current device (cached per device; racing first calls all
+// store the same value).
+cudaError_t current_sm_count(int* out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (cached > 0) { *out = cached; return cudaSuccess; }
+    }
+    int sms = 0;
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(sms, std::memory_order_relaxed);
+    *out = sms;
+    return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+struct Range {
+    const void* p;
+    uint64_t bytes;
+};
+
+bool overlap(Range a, Range b) {
+    if (a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+bool any_overlap(std::initializer_list<Range> outs, std::initializer_list<Range> ins) {
+    for (auto o = outs.begin(); o != outs.end(); ++o) {
+        for (const Range& i : ins)
+            if (overlap(*o, i)) return true;
+        for (auto o2 = o + 1; o2 != outs.end(); ++o2)
+            if (overlap(*o, *o2)) return true;
+    }
+    return false;
+}
+
+moe_status_t check_route_sizes(int64_t T, int E, int k) {
+    if (T < 0 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+    if (E > MOE_MAX_EXPERTS || k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
+    if (T * int64_t(k) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+// Rows of bfloat16 vectors: width a multiple of 8 elements (16 bytes).
+moe_status_t check_rows(int64_t rows, int width, int64_t slots_mult) {
+    if (rows < 0 || width < 1) return MOE_ERR_INVALID_ARG;
+    if (width % 8 != 0) return MOE_ERR_MISALIGNED;
+    if (rows * slots_mult >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status_t from_cuda(cudaError_t err) { return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_route_workspace_size(int64_t T, int E, int k, size_t* bytes) {
+    if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+    const moe_status_t st = check_route_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    *bytes = T == 0 ? 0 : moe::plan_route(T, E, k).ws_bytes;
+    return MOE_OK;
+}
+
+moe_status_t moe_route(const float* logits, int64_t T, int E, int k, int renorm,
+                       int32_t* topk_ids, float* topk_weights, int32_t* expert_counts,
+                       int32_t* expert_offsets, int32_t* perm, int32_t* inv_perm,
+                       void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    moe_status_t st = check_route_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    if (expert_counts == nullptr || expert_offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned4(expert_counts) || !aligned4(expert_offsets)) return MOE_ERR_MISALIGNED;
+    const uint64_t S = uint64_t(T) * uint64_t(k);
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        if (any_overlap({{expert_counts, 4ull * E}, {expert_offsets, 4ull * (E + 1)}}, {}))
+            return MOE_ERR_INVALID_ARG;
+        cudaError_t err = cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s);
+        if (err == cudaSuccess) err = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s);
+        return from_cuda(err);
+    }
+    if (logits == nullptr || topk_ids == nullptr || topk_weights == nullptr || perm == nullptr ||
+        inv_perm == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned4(logits) || !aligned4(topk_ids) || !aligned4(topk_weights) || !aligned4(perm) ||
+        !aligned4(inv_perm))
+        return MOE_ERR_MISALIGNED;
+    const RoutePlan plan = moe::plan_route(T, E, k);
+    if (plan.ws_bytes > 0) {
+        if (workspace == nullptr || workspace_bytes < plan.ws_bytes) return MOE_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return MOE_ERR_MISALIGNED;
+    }
+    const uint64_t ws = plan.ws_bytes;
+    if (any_overlap({{topk_ids, 4 * S}, {topk_weights, 4 * S}, {expert_counts, 4ull * E},
+                     {expert_offsets, 4ull * (E + 1)}, {perm, 4 * S}, {inv_perm, 4 * S},
+                     {workspace, ws}},
+                    {{logits, 4ull * uint64_t(T) * E}}))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_route(plan, logits, int(T), E, k, renorm ? 1 : 0, topk_ids,
+                                       topk_weights, expert_counts, expert_offsets, perm, inv_perm,
+                                       workspace, s));
+}
+
+moe_status_t moe_expand(const moe_bf16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
+                        moe_bf16_t* expanded_x, moe_stream_t stream) {
+    if (k < 1) return MOE_ERR_INVALID_ARG;
+    if (k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
+    moe_status_t st = check_rows(T, H, k);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    if (x == nullptr || inv_perm == nullptr || expanded_x == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(expanded_x) || !aligned4(inv_perm)) return MOE_ERR_MISALIGNED;
+    const uint64_t S = uint64_t(T) * uint64_t(k);
+    if (any_overlap({{expanded_x, 2 * S * uint64_t(H)}},
+                    {{x, 2 * uint64_t(T) * uint64_t(H)}, {inv_perm, 4 * S}}))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    cudaError_t err = current_sm_count(&sms);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_expand(x, T, H, k, inv_perm, expanded_x, sms,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_swiglu(const moe_bf16_t* gate_up, int64_t rows, int I, moe_bf16_t* act,
+                        moe_stream_t stream) {
+    moe_status_t st = check_rows(rows, I, 1);
+    if (st != MOE_OK) return st;
+    if (rows == 0) return MOE_OK;
+    if (gate_up == nullptr || act == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(gate_up) || !aligned16(act)) return MOE_ERR_MISALIGNED;
+    if (any_overlap({{act, 2 * uint64_t(rows) * uint64_t(I)}},
+                    {{gate_up, 4 * uint64_t(rows) * uint64_t(I)}}))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    cudaError_t err = current_sm_count(&sms);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_swiglu(gate_up, rows, I, act, sms,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_combine(const moe_bf16_t* expert_out, int64_t T, int H, int k,
+                         const float* topk_weights, const int32_t* inv_perm, moe_bf16_t* out,
+                         moe_stream_t stream) {
+    if (k < 1) return MOE_ERR_INVALID_ARG;
+    if (k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
+    moe_status_t st = check_rows(T, H, k);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    if (expert_out == nullptr || topk_weights == nullptr || inv_perm == nullptr || out == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(expert_out) || !aligned16(out) || !aligned4(topk_weights) ||
+        !aligned4(inv_perm))
+        return MOE_ERR_MISALIGNED;
+    const uint64_t S = uint64_t(T) * uint64_t(k);
+    if (any_overlap({{out, 2 * uint64_t(T) * uint64_t(H)}},
+                    {{expert_out, 2 * S * uint64_t(H)}, {topk_weights, 4 * S}, {inv_perm, 4 * S}}))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    cudaError_t err = current_sm_count(&sms);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_combine(expert_out, T, H, k, topk_weights, inv_perm, out, sms,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+// Device-side building blocks shared by the glue kernels: raw-bit vectors,
+// wide global loads/stores written as inline PTX, bfloat16 pack/unpack, and
+// division by a loop-invariant divisor.
+#pragma once
+
+#include <cstdint>
+
+namespace moe {
+
+constexpr int kWarp = 32;
+constexpr unsigned kFull = 0xffffffffu;
+
+// A BYTES-wide vector of raw bits (16 = 8 bf16, 32 = 16 bf16).
+template <int BYTES>
+struct alignas(BYTES) Bits {
+    uint32_t w[BYTES / 4];
+};
+
+// --------------------------------------------------------------------------
+// Wide global accesses. Each is one instruction: a 128-bit access for 16-byte
+// vectors and, on sm_100 and later, a 256-bit access for 32-byte vectors
+// ("CuTeDSL at Perplexity", section "Blackwell support": Blackwell adds
+// 256-bit loads; "[FlashInfer] CUTLASS MoE kernel optimisation", section 1:
+// one 16-byte load instead of four 4-byte loads).
+// Streaming reads of data that is read once go through the non-coherent path
+// without L1 allocation; the data must stay unchanged while the kernel runs.
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ void ld_stream(Bits<16>& v, const void* p) {
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void ld_stream(Bits<32>& v, const void* p) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
+                   "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void st_global(void* p, const Bits<16>& v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_global(void* p, const Bits<32>& v) {
+    asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]),
+                    "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                 : "memory");
+}
+
+// --------------------------------------------------------------------------
+// bfloat16 <-> float32. A bfloat16 is the upper half of a float32, so the
+// widening is a shift; the narrowing uses the hardware round-to-nearest-even
+// conversion of two floats at once (cvt.rn.bf16x2.f32 puts its first source
+// in the upper half).
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// --------------------------------------------------------------------------
+// Unsigned 32-bit division by a divisor fixed for the whole launch, as a
+// multiply-high, an add and a shift (Granlund & Montgomery, "Division by
+// Invariant Integers using Multiplication", PLDI 1994, the round-up variant
+// with a 33-bit sum): with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (umulhi(m, n) + n) >> l for every 32-bit n.
+// --------------------------------------------------------------------------
+
+struct DivU32 {
+    uint32_t d;
+    uint32_t m;
+    uint32_t l;
+
+    __host__ static DivU32 make(uint32_t d_) {
+        DivU32 r;
+        r.d = d_;
+        uint32_t l = 0;
+        while ((uint64_t(1) << l) < d_) ++l;
+        r.l = l;
+        r.m = uint32_t(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d_)) / d_ + 1);
+        return r;
+    }
+
+    __device__ __forceinline__ uint32_t div(uint32_t n) const {
+        return uint32_t((uint64_t(__umulhi(m, n)) + n) >> l);
+    }
+};
+
+}  // namespace moe

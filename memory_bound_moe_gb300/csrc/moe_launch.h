@@ -1,0 +1,43 @@
+// Host-side interface between the C-ABI layer (api.cu) and the kernel
+// translation units. Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+// Launch geometry of the routing step, a pure function of (T, E, k).
+struct RoutePlan {
+    int gs = 32;        // lanes that cooperate on one token (8, 16 or 32)
+    int epl = 1;        // experts held per lane: E <= gs * epl
+    bool fused = false; // one block does everything (small T)
+    int nt = 512;       // threads per block
+    int G = 1;          // blocks of the two-kernel path
+    int tpc = 0;        // tokens per block
+    int Ep = 0;         // E rounded up to a multiple of 4 (row stride of the count matrix)
+    size_t ws_bytes = 0;
+    size_t smem_topk = 0;
+    size_t smem_scatter = 0;
+};
+
+RoutePlan plan_route(int64_t T, int E, int k);
+
+cudaError_t launch_route(const RoutePlan& plan, const float* logits, int T, int E, int k,
+                         int renorm, int32_t* topk_ids, float* topk_weights,
+                         int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
+                         int32_t* inv_perm, void* workspace, cudaStream_t stream);
+
+cudaError_t launch_expand(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
+                          uint16_t* expanded_x, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_swiglu(const uint16_t* gate_up, int64_t rows, int I, uint16_t* act,
+                          int num_sms, cudaStream_t stream);
+
+cudaError_t launch_combine(const uint16_t* expert_out, int64_t T, int H, int k,
+                           const float* topk_weights, const int32_t* inv_perm, uint16_t* out,
+                           int num_sms, cudaStream_t stream);
+
+}  // namespace moe

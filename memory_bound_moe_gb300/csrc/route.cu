@@ -1,0 +1,454 @@
+// Routing: softmax + top-k per token, per-expert histogram, exclusive scan and
+// the stable expert-sorted permutation.
+//
+// "CuTeDSL at Perplexity", section "Mixture of Experts (MoE) dispatch/combine",
+// sub-section "Local": the routing step counts the tokens of every expert and
+// gives each token a unique index inside its expert's list. For many tokens
+// the pages count per block in shared memory and aggregate the block counts in
+// global memory; for few tokens one block routes everything. Both shapes are
+// kept here, with one change: the pages hand out indices with shared-memory
+// atomics, whose order is not reproducible, while these kernels rank slots in
+// flat slot order so the permutation is deterministic.
+//
+//   two-kernel path  route_topk_kernel    G blocks: top-k of a token range,
+//                                         block histogram -> row b of the
+//                                         count matrix (workspace)
+//                    route_scatter_kernel G blocks: every block reduces the
+//                                         count matrix (totals and the prefix
+//                                         of earlier blocks), scans the totals
+//                                         into offsets and ranks its own slots
+//   one-block path   route_fused_kernel   all of the above in one block
+#include "moe_device.cuh"
+#include "moe_launch.h"
+
+#include <algorithm>
+#include <mutex>
+
+namespace moe {
+namespace {
+
+struct RouteArgs {
+    const float* logits;
+    int T, E, k, renorm;
+    int Ep;    // count-matrix row stride
+    int tpc;   // tokens per block
+    int G;     // blocks
+    int32_t* topk_ids;
+    float* topk_weights;
+    int32_t* expert_counts;
+    int32_t* expert_offsets;
+    int32_t* perm;
+    int32_t* inv_perm;
+    int32_t* ws_counts;  // [G][Ep]
+};
+
+// Order-preserving map of a float onto uint32 (larger float -> larger key).
+// -0.0 is first folded onto +0.0 so that the two compare equal. Key 0 marks
+// "empty / already taken"; every real logit maps to 1 or more (only one NaN
+// bit pattern would map to 0, and it is lifted to 1), so a pick is always a
+// valid expert.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    v = (v == 0.0f) ? 0.0f : v;
+    const uint32_t b = __float_as_uint(v);
+    return max((b & 0x80000000u) ? ~b : (b | 0x80000000u), 1u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+    uint32_t b = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+    return __uint_as_float(b);
+}
+
+// Reductions over aligned groups of GS lanes; every lane of the warp calls.
+template <int GS>
+__device__ __forceinline__ uint32_t group_max(uint32_t v) {
+    if constexpr (GS == 32) {
+        return __reduce_max_sync(kFull, v);
+    } else {
+#pragma unroll
+        for (int o = GS / 2; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
+        return v;
+    }
+}
+
+template <int GS>
+__device__ __forceinline__ uint32_t group_min(uint32_t v) {
+    if constexpr (GS == 32) {
+        return __reduce_min_sync(kFull, v);
+    } else {
+#pragma unroll
+        for (int o = GS / 2; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(kFull, v, o));
+        return v;
+    }
+}
+
+template <int GS>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = GS / 2; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// Top-k of one token by a group of GS lanes; lane gl holds experts
+// gl, gl + GS, gl + 2GS, ... (coalesced row read) as order-preserving keys
+// (the float is recovered exactly from its key). Each of the k rounds takes
+// the group maximum of the keys and, among lanes holding it, the lowest
+// expert index; the owner then drops that expert. Lane j < k keeps the j-th
+// pick and writes it. Every lane of the warp must call (valid may differ
+// between groups of one warp; invalid groups compute on empty keys and write
+// nothing).
+template <int GS, int EPL>
+__device__ __forceinline__ void topk_token(const RouteArgs& a, int t, bool valid, int gl,
+                                           int32_t* s_hist) {
+    uint32_t key[EPL];
+    const float* row = a.logits + (size_t)t * a.E;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = gl + GS * i;
+        key[i] = (valid && e < a.E) ? order_key(__ldg(row + e)) : 0u;
+    }
+
+    // Softmax denominator over all E experts (only without renormalisation),
+    // taken before the picks remove keys.
+    float z = 0.0f;
+    if (!a.renorm) {
+        uint32_t lmax = key[0];
+#pragma unroll
+        for (int i = 1; i < EPL; ++i) lmax = max(lmax, key[i]);
+        const float vmax = key_value(group_max<GS>(lmax));
+#pragma unroll
+        for (int i = 0; i < EPL; ++i)
+            if (key[i] != 0u) z += expf(key_value(key[i]) - vmax);
+        z = group_sum<GS>(z);
+    }
+
+    int my_id = 0;
+    float my_val = 0.0f;
+    float vmax = 0.0f;
+    for (int j = 0; j < a.k; ++j) {
+        uint32_t bk = key[0];
+        int bi = 0;
+#pragma unroll
+        for (int i = 1; i < EPL; ++i) {
+            if (key[i] > bk) { bk = key[i]; bi = i; }
+        }
+        const uint32_t gk = group_max<GS>(bk);
+        const uint32_t cand = (bk == gk) ? uint32_t(gl + GS * bi) : 0xffffffffu;
+        const uint32_t ge = group_min<GS>(cand);
+        if (int(ge % GS) == gl) {
+            const int wi = int(ge / GS);
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) if (i == wi) key[i] = 0u;
+        }
+        const float gv = key_value(gk);
+        if (j == 0) vmax = gv;
+        if (gl == j) { my_id = int(ge); my_val = gv; }
+    }
+
+    // Weights in float32. The largest logit is the first pick.
+    const bool mine = gl < a.k;
+    const float ej = mine ? expf(my_val - vmax) : 0.0f;
+    const float denom = a.renorm ? group_sum<GS>(ej)   // sum over the k picks
+                                 : z;                  // sum over all E experts
+    if (valid && mine) {
+        a.topk_ids[(size_t)t * a.k + gl] = my_id;
+        a.topk_weights[(size_t)t * a.k + gl] = ej / denom;
+        atomicAdd(&s_hist[my_id], 1);
+    }
+}
+
+// Tokens [t0, t1) by a block of NT threads, GS lanes per token; the loop is
+// uniform across each warp so the group reductions see full warps.
+template <int GS, int EPL, int NT>
+__device__ __forceinline__ void topk_range(const RouteArgs& a, int t0, int t1, int32_t* s_hist) {
+    constexpr int GPW = kWarp / GS;
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    const int grp = lane / GS;
+    const int gl = lane % GS;
+    for (int tb = t0 + warp * GPW; tb < t1; tb += (NT / kWarp) * GPW) {
+        const int t = tb + grp;
+        topk_token<GS, EPL>(a, t, t < t1, gl, s_hist);
+    }
+}
+
+// Exclusive scan of in[0..n) into out[0..n) (may alias) by a block of NT
+// threads, n <= MOE_MAX_EXPERTS; returns the total. Uses s_warp[32].
+template <int NT>
+__device__ int block_exclusive_scan(const int32_t* in, int32_t* out, int n, int32_t* s_warp) {
+    constexpr int ITEMS = (1024 + NT - 1) / NT;
+    constexpr int NW = NT / kWarp;
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    const int base = threadIdx.x * ITEMS;
+    int v[ITEMS];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+        v[i] = (base + i < n) ? in[base + i] : 0;
+        local += v[i];
+    }
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == kWarp - 1) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < NW ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, w, o);
+            if (lane >= o) w += y;
+        }
+        s_warp[lane] = w;
+    }
+    __syncthreads();
+    int run = (warp > 0 ? s_warp[warp - 1] : 0) + x - local;
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+        if (base + i < n) out[base + i] = run;
+        run += v[i];
+    }
+    const int total = s_warp[NW - 1];
+    __syncthreads();
+    return total;
+}
+
+// Stable rank of the slots [s0, s1) inside their experts. s_base[e] is the
+// first row of expert e owned by this block; s_wstart is [NW][E] scratch.
+// The slots are split into one contiguous run per warp (a multiple of 32);
+// pass 1 counts each warp's slots per expert, a scan over warps turns the
+// counts into per-warp starting rows, pass 2 ranks each 32-slot chunk with
+// __match_any_sync (lanes with the same expert) and the popcount of the
+// lower-lane peers, then advances the warp's counter. Slot order decides the
+// rank, so the result is deterministic.
+template <int NT>
+__device__ void scatter_slots(const RouteArgs& a, int s0, int s1, const int32_t* s_base,
+                              int32_t* s_wstart) {
+    constexpr int NW = NT / kWarp;
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    const int E = a.E;
+    const int n = s1 - s0;
+    const int per = (((n + NW - 1) / NW) + kWarp - 1) / kWarp * kWarp;
+    const int lo = s0 + warp * per;
+    const int hi = min(s1, lo + per);
+    int32_t* mine = s_wstart + (size_t)warp * E;
+    const unsigned lower = (1u << lane) - 1u;
+
+    for (int e = lane; e < E; e += kWarp) mine[e] = 0;
+    __syncwarp();
+    for (int c = lo; c < hi; c += kWarp) {
+        const int s = c + lane;
+        const int e = (s < hi) ? __ldcg(a.topk_ids + s) : -1;
+        const unsigned peers = __match_any_sync(kFull, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += NT) {
+        int run = s_base[e];
+        for (int w = 0; w < NW; ++w) {
+            const int v = s_wstart[(size_t)w * E + e];
+            s_wstart[(size_t)w * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int c = lo; c < hi; c += kWarp) {
+        const int s = c + lane;
+        const int e = (s < hi) ? __ldcg(a.topk_ids + s) : -1;
+        const unsigned peers = __match_any_sync(kFull, e);
+        if (e >= 0) {
+            const int p = mine[e] + __popc(peers & lower);
+            a.perm[p] = s;
+            a.inv_perm[s] = p;
+        }
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+template <int GS, int EPL, int NT>
+__global__ void __launch_bounds__(NT) route_topk_kernel(RouteArgs a) {
+    extern __shared__ int32_t smem[];
+    int32_t* s_hist = smem;  // [Ep]
+    for (int e = threadIdx.x; e < a.Ep; e += NT) s_hist[e] = 0;
+    __syncthreads();
+    const int t0 = blockIdx.x * a.tpc;
+    const int t1 = min(a.T, t0 + a.tpc);
+    topk_range<GS, EPL, NT>(a, t0, t1, s_hist);
+    __syncthreads();
+    int32_t* row = a.ws_counts + (size_t)blockIdx.x * a.Ep;
+    for (int e = threadIdx.x; e < a.Ep; e += NT) row[e] = s_hist[e];
+}
+
+// Scatter-kernel shared memory, in int32 words.
+__host__ __device__ inline int scatter_rowgroups(int Ep, int nt) {
+    const int cg = Ep / 4;
+    return cg >= nt ? 1 : nt / cg;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) route_scatter_kernel(RouteArgs a) {
+    extern __shared__ int32_t smem[];
+    const int Ep = a.Ep;
+    const int CG = Ep / 4;
+    const int R = scatter_rowgroups(Ep, NT);
+    int32_t* s_ptot = smem;                 // [R][Ep]
+    int32_t* s_ppre = s_ptot + R * Ep;      // [R][Ep]
+    int32_t* s_tot = s_ppre + R * Ep;       // [Ep]
+    int32_t* s_base = s_tot + Ep;           // [Ep]
+    int32_t* s_warp = s_base + Ep;          // [32]
+    int32_t* s_wstart = s_warp + 32;        // [NW][E]
+    const int b = blockIdx.x;
+
+    // Column sums of the count matrix: all blocks (totals) and blocks before
+    // this one (prefix). Rows are interleaved over R row groups, columns are
+    // read as int4 so each warp reads contiguous 512-byte runs.
+    for (int idx = threadIdx.x; idx < R * CG; idx += NT) {
+        const int r = idx / CG;
+        const int cg = idx % CG;
+        int4 tot = make_int4(0, 0, 0, 0), pre = make_int4(0, 0, 0, 0);
+        for (int rb = r; rb < a.G; rb += R) {
+            const int4 v = __ldg(reinterpret_cast<const int4*>(a.ws_counts + (size_t)rb * Ep) + cg);
+            tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
+            if (rb < b) { pre.x += v.x; pre.y += v.y; pre.z += v.z; pre.w += v.w; }
+        }
+        reinterpret_cast<int4*>(s_ptot + r * Ep)[cg] = tot;
+        reinterpret_cast<int4*>(s_ppre + r * Ep)[cg] = pre;
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < Ep; c += NT) {
+        int tot = 0, pre = 0;
+        for (int r = 0; r < R; ++r) { tot += s_ptot[r * Ep + c]; pre += s_ppre[r * Ep + c]; }
+        s_tot[c] = tot;
+        s_base[c] = pre;
+    }
+    __syncthreads();
+    if (b == 0) {
+        for (int e = threadIdx.x; e < a.E; e += NT) a.expert_counts[e] = s_tot[e];
+    }
+    block_exclusive_scan<NT>(s_tot, s_tot, a.E, s_warp);   // s_tot := offsets
+    for (int e = threadIdx.x; e < a.E; e += NT) {
+        if (b == 0) a.expert_offsets[e] = s_tot[e];
+        s_base[e] += s_tot[e];
+    }
+    if (b == 0 && threadIdx.x == 0) a.expert_offsets[a.E] = a.T * a.k;
+    __syncthreads();
+
+    const int t0 = b * a.tpc;
+    const int t1 = min(a.T, t0 + a.tpc);
+    scatter_slots<NT>(a, t0 * a.k, t1 * a.k, s_base, s_wstart);
+}
+
+template <int GS, int EPL, int NT>
+__global__ void __launch_bounds__(NT) route_fused_kernel(RouteArgs a) {
+    extern __shared__ int32_t smem[];
+    const int Ep = a.Ep;
+    int32_t* s_hist = smem;            // [Ep] counts, then offsets
+    int32_t* s_warp = s_hist + Ep;     // [32]
+    int32_t* s_wstart = s_warp + 32;   // [NW][E]
+    for (int e = threadIdx.x; e < Ep; e += NT) s_hist[e] = 0;
+    __syncthreads();
+    topk_range<GS, EPL, NT>(a, 0, a.T, s_hist);
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += NT) a.expert_counts[e] = s_hist[e];
+    block_exclusive_scan<NT>(s_hist, s_hist, a.E, s_warp);
+    for (int e = threadIdx.x; e < a.E; e += NT) a.expert_offsets[e] = s_hist[e];
+    if (threadIdx.x == 0) a.expert_offsets[a.E] = a.T * a.k;
+    __syncthreads();
+    scatter_slots<NT>(a, 0, a.T * a.k, s_hist, s_wstart);
+}
+
+constexpr int kNtSplit = 512;
+constexpr int kNtFused = 1024;
+
+template <typename K>
+cudaError_t allow_smem(K kernel, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+}
+
+template <int GS, int EPL>
+cudaError_t launch_route_t(const RoutePlan& p, const RouteArgs& a, cudaStream_t stream) {
+    cudaError_t err;
+    if (p.fused) {
+        auto kf = route_fused_kernel<GS, EPL, kNtFused>;
+        if ((err = allow_smem(kf, p.smem_topk)) != cudaSuccess) return err;
+        kf<<<1, kNtFused, p.smem_topk, stream>>>(a);
+        return cudaGetLastError();
+    }
+    auto k1 = route_topk_kernel<GS, EPL, kNtSplit>;
+    auto k2 = route_scatter_kernel<kNtSplit>;
+    if ((err = allow_smem(k1, p.smem_topk)) != cudaSuccess) return err;
+    if ((err = allow_smem(k2, p.smem_scatter)) != cudaSuccess) return err;
+    k1<<<p.G, kNtSplit, p.smem_topk, stream>>>(a);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    k2<<<p.G, kNtSplit, p.smem_scatter, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+RoutePlan plan_route(int64_t T, int E, int k) {
+    (void)k;
+    RoutePlan p;
+    if (E <= 8) { p.gs = 8; p.epl = 1; }
+    else if (E <= 16) { p.gs = 16; p.epl = 1; }
+    else { p.gs = 32; p.epl = (E + 31) / 32; }
+    if (p.epl > 2) p.epl = p.epl <= 4 ? 4 : p.epl <= 8 ? 8 : p.epl <= 16 ? 16 : 32;
+    p.Ep = (E + 3) / 4 * 4;
+    const int fused_groups = (kNtFused / kWarp) * (kWarp / p.gs);
+    p.fused = T <= 2 * fused_groups;
+    if (p.fused) {
+        p.nt = kNtFused;
+        p.G = 1;
+        p.tpc = int(T);
+        p.ws_bytes = 0;
+        p.smem_topk = sizeof(int32_t) * (size_t(p.Ep) + 32 + size_t(kNtFused / kWarp) * E);
+        return p;
+    }
+    p.nt = kNtSplit;
+    const int groups = (kNtSplit / kWarp) * (kWarp / p.gs);
+    const int gmax = std::max(1, std::min(128, 32768 / p.Ep));
+    int64_t tpc = std::max<int64_t>(groups, (T + gmax - 1) / gmax);
+    p.tpc = int(tpc);
+    p.G = int((T + tpc - 1) / tpc);
+    p.ws_bytes = sizeof(int32_t) * size_t(p.G) * size_t(p.Ep);
+    p.smem_topk = sizeof(int32_t) * size_t(p.Ep);
+    const int R = scatter_rowgroups(p.Ep, kNtSplit);
+    p.smem_scatter = sizeof(int32_t) *
+        (size_t(2) * R * p.Ep + 2 * size_t(p.Ep) + 32 + size_t(kNtSplit / kWarp) * E);
+    return p;
+}
+
+cudaError_t launch_route(const RoutePlan& plan, const float* logits, int T, int E, int k,
+                         int renorm, int32_t* topk_ids, float* topk_weights,
+                         int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
+                         int32_t* inv_perm, void* workspace, cudaStream_t stream) {
+    RouteArgs a;
+    a.logits = logits;
+    a.T = T; a.E = E; a.k = k; a.renorm = renorm;
+    a.Ep = plan.Ep; a.tpc = plan.tpc; a.G = plan.G;
+    a.topk_ids = topk_ids; a.topk_weights = topk_weights;
+    a.expert_counts = expert_counts; a.expert_offsets = expert_offsets;
+    a.perm = perm; a.inv_perm = inv_perm;
+    a.ws_counts = static_cast<int32_t*>(workspace);
+    switch (plan.gs * 100 + plan.epl) {
+        case 801: return launch_route_t<8, 1>(plan, a, stream);
+        case 1601: return launch_route_t<16, 1>(plan, a, stream);
+        case 3201: return launch_route_t<32, 1>(plan, a, stream);
+        case 3202: return launch_route_t<32, 2>(plan, a, stream);
+        case 3204: return launch_route_t<32, 4>(plan, a, stream);
+        case 3208: return launch_route_t<32, 8>(plan, a, stream);
+        case 3216: return launch_route_t<32, 16>(plan, a, stream);
+        case 3232: return launch_route_t<32, 32>(plan, a, stream);
+        default: return cudaErrorInvalidConfiguration;
+    }
+}
+
+}  // namespace moe

@@ -1,0 +1,101 @@
+// SwiGLU activation over the fc1 output (doActivation).
+//
+// "[FlashInfer] CUTLASS MoE kernel optimisation" (flashinfer PR #3761),
+// section 1 "Explicit vectorization" (one wide load/store per vector instead
+// of several narrow ones) and section 2 "Dynamic threads" (the fixed
+// 256-thread, one-row-per-block launch idled most warps at intermediate size
+// 768). Here the rows are flattened: consecutive threads take consecutive
+// 16- or 32-byte vectors of act, whatever the row width, and a grid of one
+// wave of resident blocks sweeps the whole [rows, I] output, so every SM stays
+// busy for any I and no block shape depends on I.
+//
+//   act[r, i] = bf16_rn( silu(g) * u ), g = gate_up[r, i], u = gate_up[r, I + i],
+//   silu(g) = g / (1 + e^-g) in float32 (fast exp and reciprocal).
+#include "moe_device.cuh"
+#include "moe_launch.h"
+#include "rows_common.cuh"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+template <int VB>
+__device__ __forceinline__ void swiglu_vec(const Bits<VB>& g, const Bits<VB>& u, Bits<VB>& o) {
+#pragma unroll
+    for (int w = 0; w < VB / 4; ++w) {
+        const float lo = silu_mul(bf16_lo(g.w[w]), bf16_lo(u.w[w]));
+        const float hi = silu_mul(bf16_hi(g.w[w]), bf16_hi(u.w[w]));
+        o.w[w] = pack_bf16x2(lo, hi);
+    }
+}
+
+// Item v = r * nv + c is the c-th VB-byte vector of act row r. Each thread
+// issues U items' loads before any math (2U wide loads in flight).
+template <int VB, int U, int NT>
+__global__ void __launch_bounds__(NT) swiglu_kernel(const uint8_t* __restrict__ gate_up,
+                                                    uint8_t* __restrict__ act, uint32_t total,
+                                                    DivU32 nv, uint32_t in_row_bytes,
+                                                    uint32_t out_row_bytes) {
+    const uint32_t stride = gridDim.x * NT * U;
+    for (uint32_t base = blockIdx.x * NT * U + threadIdx.x; base < total; base += stride) {
+        Bits<VB> g[U], u[U];
+        uint64_t dst[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const uint32_t v = base + i * NT;
+            if (v < total) {
+                const uint32_t r = nv.div(v);
+                const uint32_t c = v - r * nv.d;
+                const uint8_t* src = gate_up + uint64_t(r) * in_row_bytes + uint64_t(c) * VB;
+                ld_stream(g[i], src);
+                ld_stream(u[i], src + out_row_bytes);
+                dst[i] = uint64_t(r) * out_row_bytes + uint64_t(c) * VB;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            if (base + i * NT < total) {
+                Bits<VB> o;
+                swiglu_vec<VB>(g[i], u[i], o);
+                st_global(act + dst[i], o);
+            }
+        }
+    }
+}
+
+constexpr int kNt = 256;
+constexpr int kUnroll = 2;
+
+template <int VB>
+cudaError_t launch_vb(const uint16_t* gate_up, int64_t rows, int I, uint16_t* act, int num_sms,
+                      cudaStream_t stream) {
+    auto kernel = swiglu_kernel<VB, kUnroll, kNt>;
+    const uint32_t nv = uint32_t(uint64_t(I) * 2 / VB);
+    const int64_t rows_per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / nv));
+    for (int64_t r0 = 0; r0 < rows; r0 += rows_per_launch) {
+        const int64_t nr = std::min(rows_per_launch, rows - r0);
+        const uint32_t total = uint32_t(nr * nv);
+        const int grid = grid_for(kernel, kNt, total, uint64_t(kNt) * kUnroll, num_sms);
+        kernel<<<grid, kNt, 0, stream>>>(
+            reinterpret_cast<const uint8_t*>(gate_up + r0 * 2 * int64_t(I)),
+            reinterpret_cast<uint8_t*>(act + r0 * int64_t(I)), total, DivU32::make(nv),
+            uint32_t(4 * int64_t(I)), uint32_t(2 * int64_t(I)));
+        const cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_swiglu(const uint16_t* gate_up, int64_t rows, int I, uint16_t* act,
+                          int num_sms, cudaStream_t stream) {
+    if (can_use_32b(uint64_t(I) * 2, {gate_up, act}))
+        return launch_vb<32>(gate_up, rows, I, act, num_sms, stream);
+    return launch_vb<16>(gate_up, rows, I, act, num_sms, stream);
+}
+
+}  // namespace moe

@@ -1,0 +1,152 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+``include/*.h`` declares, and its host-side validation rejects bad arguments
+before any CUDA call (only fake, never-dereferenced addresses are passed, and
+every call here returns before a launch)."""
+from __future__ import annotations
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+OK, INVALID, MISALIGNED, UNSUPPORTED, WORKSPACE, CUDA = range(6)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from memory_bound_moe_gb300 import build as b
+    b.build()
+    import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+    from memory_bound_moe_gb300 import binding
+    return binding.load_library()
+
+
+def _declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"moe_route", "moe_expand", "moe_swiglu", "moe_combine",
+            "moe_route_workspace_size", "moe_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_MISALIGNED",
+                                 "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE", "MOE_ERR_CUDA"]):
+        assert lib.moe_status_string(code).decode() == name
+    assert lib.moe_status_string(99).decode() == "MOE_ERR_UNKNOWN"
+
+
+def _ws(lib, T, E, k):
+    out = ctypes.c_size_t(12345)
+    st = lib.moe_route_workspace_size(T, E, k, ctypes.byref(out))
+    return st, out.value
+
+
+def test_workspace_size_rules(lib):
+    assert _ws(lib, 0, 8, 2) == (OK, 0)
+    assert _ws(lib, 16, 256, 8) == (OK, 0)          # one-block path: no workspace
+    st, b = _ws(lib, 4096, 128, 8)
+    assert st == OK and b > 0 and b % 16 == 0
+    st2, b2 = _ws(lib, 4096, 128, 8)
+    assert (st2, b2) == (st, b)                       # pure function
+    assert _ws(lib, 8192, 8, 2)[0] == OK
+    assert _ws(lib, -1, 8, 2)[0] == INVALID
+    assert _ws(lib, 10, 8, 9)[0] == INVALID           # k > E
+    assert _ws(lib, 10, 8, 0)[0] == INVALID
+    assert _ws(lib, 10, 2048, 8)[0] == UNSUPPORTED    # E > 1024
+    assert _ws(lib, 10, 64, 17)[0] == UNSUPPORTED     # k > 16
+    assert _ws(lib, 2 ** 31 // 4, 64, 4)[0] == UNSUPPORTED
+    assert lib.moe_route_workspace_size(10, 8, 2, None) == INVALID
+
+
+# Fake device addresses, far apart and 256-byte aligned; never dereferenced.
+A = [0x7f0000000000 + i * 0x100000000 for i in range(16)]
+
+
+def _route(lib, T=64, E=8, k=2, ptrs=None, ws=0, ws_bytes=0):
+    p = list(A[:7]) if ptrs is None else ptrs
+    return lib.moe_route(p[0], T, E, k, 1, p[1], p[2], p[3], p[4], p[5], p[6], ws, ws_bytes, None)
+
+
+def test_route_rejects_bad_arguments(lib):
+    assert _route(lib, k=9) == INVALID
+    assert _route(lib, k=0) == INVALID
+    assert _route(lib, T=-3) == INVALID
+    assert _route(lib, E=2000, k=2) == UNSUPPORTED
+    assert _route(lib, E=64, k=20) == UNSUPPORTED
+    for i in range(7):
+        p = list(A[:7])
+        p[i] = 0
+        assert _route(lib, ptrs=p) == INVALID, i
+        p = list(A[:7])
+        p[i] += 2                                     # not 4-byte aligned
+        assert _route(lib, ptrs=p) == MISALIGNED, i
+    # two-kernel path needs a workspace
+    st, need = _ws(lib, 4096, 128, 8)
+    assert _route(lib, T=4096, E=128, k=8) == WORKSPACE
+    assert _route(lib, T=4096, E=128, k=8, ws=A[8], ws_bytes=need - 1) == WORKSPACE
+    assert _route(lib, T=4096, E=128, k=8, ws=A[8] + 4, ws_bytes=need) == MISALIGNED
+    # outputs overlapping the logits or each other
+    p = list(A[:7])
+    p[1] = A[0] + 64
+    assert _route(lib, ptrs=p) == INVALID
+    p = list(A[:7])
+    p[6] = p[5] + 8
+    assert _route(lib, ptrs=p) == INVALID
+
+
+def test_expand_swiglu_combine_reject_bad_arguments(lib):
+    # expand(x, T, H, k, inv_perm, out, stream)
+    assert lib.moe_expand(A[0], 16, 256, 0, A[1], A[2], None) == INVALID
+    assert lib.moe_expand(A[0], 16, 256, 17, A[1], A[2], None) == UNSUPPORTED
+    assert lib.moe_expand(A[0], 16, 250, 2, A[1], A[2], None) == MISALIGNED   # H % 8
+    assert lib.moe_expand(A[0] + 8, 16, 256, 2, A[1], A[2], None) == MISALIGNED
+    assert lib.moe_expand(A[0], 16, 256, 2, A[1] + 1, A[2], None) == MISALIGNED
+    assert lib.moe_expand(0, 16, 256, 2, A[1], A[2], None) == INVALID
+    assert lib.moe_expand(A[0], -1, 256, 2, A[1], A[2], None) == INVALID
+    assert lib.moe_expand(A[0], 16, 256, 2, A[1], A[0] + 256, None) == INVALID  # out over x
+    assert lib.moe_expand(0, 0, 256, 2, 0, 0, None) == OK                       # empty batch
+    # swiglu(gate_up, rows, I, act, stream)
+    assert lib.moe_swiglu(A[0], 16, 100, A[1], None) == MISALIGNED             # I % 8
+    assert lib.moe_swiglu(A[0], 16, 0, A[1], None) == INVALID
+    assert lib.moe_swiglu(A[0] + 4, 16, 128, A[1], None) == MISALIGNED
+    assert lib.moe_swiglu(A[0], 16, 128, 0, None) == INVALID
+    assert lib.moe_swiglu(A[0], 16, 128, A[0] + 1024, None) == INVALID         # act over gate_up
+    assert lib.moe_swiglu(0, 0, 128, 0, None) == OK
+    # combine(expert_out, T, H, k, w, inv_perm, out, stream)
+    assert lib.moe_combine(A[0], 16, 256, 2, A[1], A[2], A[3] + 8, None) == MISALIGNED
+    assert lib.moe_combine(A[0], 16, 256, 2, A[1] + 2, A[2], A[3], None) == MISALIGNED
+    assert lib.moe_combine(A[0], 16, 256, 2, 0, A[2], A[3], None) == INVALID
+    assert lib.moe_combine(A[0], 16, 264, 0, A[1], A[2], A[3], None) == INVALID
+    assert lib.moe_combine(A[0], 16, 260, 2, A[1], A[2], A[3], None) == MISALIGNED
+    assert lib.moe_combine(A[0], 16, 256, 2, A[1], A[2], A[1], None) == INVALID  # out over w
+    assert lib.moe_combine(0, 0, 256, 2, 0, 0, 0, None) == OK
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    from memory_bound_moe_gb300 import moe_swiglu
+    with pytest.raises(ValueError):
+        moe_swiglu(torch.zeros((4, 16), dtype=torch.bfloat16))
+
+
+def test_product_path_never_imports_the_oracle():
+    # the oracle is test infrastructure: nothing in the package loads or calls it
+    pat = re.compile(r"\b(import|from)\s+oracle\b|\boracle\.\w+\(|moe_oracle|liboracle|\boracle_\w+\(")
+    pkg = os.path.join(ROOT, "memory_bound_moe_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*.*"), recursive=True):
+        if path.endswith((".py", ".cu", ".cuh", ".h")):
+            assert not pat.search(open(path).read()), path

@@ -1,0 +1,58 @@
+"""The N > 1 bench path on CPU: two gloo ranks, each a replica with its own
+batch (no collective on the data path); only the step time is reduced (max
+over ranks) and the job throughput counts every rank's tokens."""
+from __future__ import annotations
+
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    bench._PG["on"] = True
+    local_ms = [0.25, 0.40][rank]            # a slower second rank
+    ms = bench.reduce_max(local_ms)
+    value = bench.job_throughput(world, 4096, ms)
+    # replicas draw different batches: the seed is the rank
+    from memory_bound_moe_gb300.workloads import WORKLOADS, generate
+    logits = generate(WORKLOADS["tiny"], seed=rank, parts=("logits",))["logits"]
+    q.put((rank, ms, value, float(logits[0, 0])))
+    bench.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_and_throughput():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res[0][1] == res[1][1] == pytest.approx(0.40)
+    assert res[0][2] == pytest.approx(2 * 4096 / 0.40e-3)
+    assert res[0][3] != res[1][3]
+
+
+def test_single_rank_reduce_is_identity():
+    import bench
+    assert bench.reduce_max(1.5) == 1.5
+    assert bench.job_throughput(1, 4096, 0.1) == pytest.approx(4096 / 1e-4)
