@@ -126,6 +126,41 @@ moe_status_t moe_route(const float* logits, int64_t T, int E, int k, int renorm,
                        moe_stream_t stream);
 
 /*
+ * moe_route without a caller-provided workspace: the same computation,
+ * outputs, validation and status codes as moe_route, with the routing
+ * scratch held in a device array inside the library. The pages have no
+ * counterpart of this entry point.
+ *
+ * Some callers cannot allocate device memory where they route: a runtime
+ * that plans and owns all device memory at start-up and forbids allocation
+ * afterwards, an allocator-free plugin or embedding host, or a call site that
+ * cannot tolerate cudaMalloc's possible implicit synchronisation. moe_route
+ * would need such a caller to find a workspace for it; this entry point needs
+ * none and calls no allocating routine.
+ *
+ *   - The scratch is one static device array of MOE_ROUTE_STATIC_SCRATCH_BYTES
+ *     (128 KiB); every device that loads the library reserves it until the
+ *     process exits. Sizes whose workspace (moe_route_workspace_size) exceeds
+ *     it are rejected with MOE_ERR_WORKSPACE before anything is launched; no
+ *     size accepted by moe_route currently needs more than 128 KiB.
+ *   - The first call on a device (while that device is current) looks up the
+ *     array's device address and caches it; make that first call before any
+ *     stream capture on that device.
+ *   - All calls share the one array and it keeps whatever the last call left
+ *     there. Nothing in it has to start at zero: each call writes every entry
+ *     it later reads. Calls that can overlap on the GPU (different streams
+ *     without ordering between them, or several host threads) race on the
+ *     array and give wrong results; order them.
+ */
+#define MOE_ROUTE_STATIC_SCRATCH_BYTES (128u * 1024u)
+
+moe_status_t moe_route_static(const float* logits, int64_t T, int E, int k, int renorm,
+                              int32_t* topk_ids, float* topk_weights,
+                              int32_t* expert_counts, int32_t* expert_offsets,
+                              int32_t* perm, int32_t* inv_perm,
+                              moe_stream_t stream);
+
+/*
  * Row expansion into expert order (expandInputRows).
  * "CuTeDSL at Perplexity", section "Mixture of Experts (MoE) dispatch/combine",
  * sub-section "Local" (tokens are copied to the buffer the MoE GEMM reads),
