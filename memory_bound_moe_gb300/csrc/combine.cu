@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(NT) combine_kernel(const uint8_t* __restrict__
                                                      const int32_t* __restrict__ inv_perm, int k,
                                                      uint32_t S, uint32_t total, DivU32 nv,
                                                      uint32_t row_bytes) {
+    pdl_wait_and_release();
     for (uint32_t v = blockIdx.x * NT + threadIdx.x; v < total; v += gridDim.x * NT) {
         const uint32_t t = nv.div(v);
         const uint32_t c = v - t * nv.d;
@@ -85,24 +86,31 @@ __global__ void __launch_bounds__(NT) combine_kernel(const uint8_t* __restrict__
     }
 }
 
-constexpr int kNt = 256;
+#ifndef MOE_COMBINE_NT
+#define MOE_COMBINE_NT 256
+#endif
+// k below this uses 32-byte vectors (k * 8 registers of loads in flight)
+#ifndef MOE_COMBINE_WIDE_BELOW_K
+#define MOE_COMBINE_WIDE_BELOW_K 8
+#endif
+constexpr int kNt = MOE_COMBINE_NT;
 
 template <int VB, int KT>
 cudaError_t launch_t(const uint16_t* eo, int64_t T, int H, int k, const float* w,
                      const int32_t* inv_perm, uint16_t* out, int num_sms, cudaStream_t stream) {
     auto kernel = combine_kernel<VB, KT, kNt>;
+    static const int occ = resident_blocks(kernel, kNt);
     const uint32_t nv = uint32_t(uint64_t(H) * 2 / VB);
     const uint32_t S = uint32_t(T * k);
     const int64_t tok_per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / nv));
     for (int64_t t0 = 0; t0 < T; t0 += tok_per_launch) {
         const int64_t nt = std::min(tok_per_launch, T - t0);
         const uint32_t total = uint32_t(nt * nv);
-        const int grid = grid_for(kernel, kNt, total, uint64_t(kNt), num_sms);
-        kernel<<<grid, kNt, 0, stream>>>(reinterpret_cast<const uint8_t*>(eo),
-                                        reinterpret_cast<uint8_t*>(out + t0 * int64_t(H)),
-                                        w + t0 * k, inv_perm + t0 * k, k, S, total,
-                                        DivU32::make(nv), uint32_t(2 * int64_t(H)));
-        const cudaError_t err = cudaGetLastError();
+        const int grid = grid_for(occ, total, uint64_t(kNt), num_sms);
+        const cudaError_t err = launch_pdl(
+            kernel, dim3(grid), dim3(kNt), 0, stream, reinterpret_cast<const uint8_t*>(eo),
+            reinterpret_cast<uint8_t*>(out + t0 * int64_t(H)), w + t0 * k, inv_perm + t0 * k, k, S,
+            total, DivU32::make(nv), uint32_t(2 * int64_t(H)));
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
@@ -127,7 +135,7 @@ cudaError_t launch_combine(const uint16_t* expert_out, int64_t T, int H, int k,
                            int num_sms, cudaStream_t stream) {
     // 8 gathered rows of 32 bytes would hold 64 registers of loads per thread;
     // large k keeps 16-byte vectors (still k loads in flight).
-    if (k < 8 && can_use_32b(uint64_t(H) * 2, {expert_out, out}))
+    if (k < MOE_COMBINE_WIDE_BELOW_K && can_use_32b(uint64_t(H) * 2, {expert_out, out}))
         return launch_vb<32>(expert_out, T, H, k, topk_weights, inv_perm, out, num_sms, stream);
     return launch_vb<16>(expert_out, T, H, k, topk_weights, inv_perm, out, num_sms, stream);
 }

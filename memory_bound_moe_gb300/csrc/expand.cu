@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(NT) expand_kernel(const uint8_t* __restrict__ 
                                                     const int32_t* __restrict__ inv_perm, int k,
                                                     uint32_t S, uint32_t total, DivU32 nv,
                                                     uint32_t row_bytes) {
+    pdl_wait_and_release();
     const uint32_t stride = gridDim.x * NT * U;
     for (uint32_t base = blockIdx.x * NT * U + threadIdx.x; base < total; base += stride) {
         Bits<VB> val[U];
@@ -50,25 +51,31 @@ __global__ void __launch_bounds__(NT) expand_kernel(const uint8_t* __restrict__ 
     }
 }
 
-constexpr int kNt = 256;
-constexpr int kUnroll = 2;
+#ifndef MOE_EXPAND_NT
+#define MOE_EXPAND_NT 256
+#endif
+#ifndef MOE_EXPAND_UNROLL
+#define MOE_EXPAND_UNROLL 2
+#endif
+constexpr int kNt = MOE_EXPAND_NT;
+constexpr int kUnroll = MOE_EXPAND_UNROLL;
 
 template <int VB>
 cudaError_t launch_vb(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
                       uint16_t* out, int num_sms, cudaStream_t stream) {
     auto kernel = expand_kernel<VB, kUnroll, kNt>;
+    static const int occ = resident_blocks(kernel, kNt);
     const uint32_t nv = uint32_t(uint64_t(H) * 2 / VB);
     const uint32_t S = uint32_t(T * k);
     const int64_t tok_per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / nv));
     for (int64_t t0 = 0; t0 < T; t0 += tok_per_launch) {
         const int64_t nt = std::min(tok_per_launch, T - t0);
         const uint32_t total = uint32_t(nt * nv);
-        const int grid = grid_for(kernel, kNt, total, uint64_t(kNt) * kUnroll, num_sms);
-        kernel<<<grid, kNt, 0, stream>>>(
-            reinterpret_cast<const uint8_t*>(x + t0 * int64_t(H)),
-            reinterpret_cast<uint8_t*>(out), inv_perm + t0 * k, k, S, total, DivU32::make(nv),
-            uint32_t(2 * int64_t(H)));
-        const cudaError_t err = cudaGetLastError();
+        const int grid = grid_for(occ, total, uint64_t(kNt) * kUnroll, num_sms);
+        const cudaError_t err = launch_pdl(
+            kernel, dim3(grid), dim3(kNt), 0, stream,
+            reinterpret_cast<const uint8_t*>(x + t0 * int64_t(H)), reinterpret_cast<uint8_t*>(out),
+            inv_perm + t0 * k, k, S, total, DivU32::make(nv), uint32_t(2 * int64_t(H)));
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;

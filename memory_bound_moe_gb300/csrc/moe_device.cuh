@@ -69,6 +69,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // --------------------------------------------------------------------------
+// Programmatic dependent launch (sm_90 and later; "CuTeDSL at Perplexity",
+// section "Grid synchronization", notes that it cuts launch overhead from
+// Hopper on). Kernels launched with launch_pdl() may be scheduled while the
+// previous kernel in the stream is still running: each such kernel first
+// waits, before touching global memory, until that kernel has completed and
+// its writes are visible, and signals right away that the next kernel may be
+// scheduled. Both instructions return at once when there is no programmatic
+// dependency, and the wait always ends (the previous kernel always ends).
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ void pdl_wait_and_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// --------------------------------------------------------------------------
 // Unsigned 32-bit division by a divisor fixed for the whole launch, as a
 // multiply-high, an add and a shift (Granlund & Montgomery, "Division by
 // Invariant Integers using Multiplication", PLDI 1994, the round-up variant

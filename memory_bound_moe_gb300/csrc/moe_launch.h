@@ -17,6 +17,7 @@ struct RoutePlan {
     int nt = 512;       // threads per block
     int G = 1;          // blocks of the two-kernel path
     int tpc = 0;        // tokens per block
+    int tpw = 0;        // tokens per warp (contiguous run inside the block)
     int Ep = 0;         // E rounded up to a multiple of 4 (row stride of the count matrix)
     size_t ws_bytes = 0;
     size_t smem_topk = 0;

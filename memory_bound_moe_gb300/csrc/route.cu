@@ -8,21 +8,32 @@
 // global memory; for few tokens one block routes everything. Both shapes are
 // kept here, with one change: the pages hand out indices with shared-memory
 // atomics, whose order is not reproducible, while these kernels rank slots in
-// flat slot order so the permutation is deterministic.
+// flat slot order (s = t*k + j) so the permutation is deterministic.
 //
-//   two-kernel path  route_topk_kernel    G blocks: top-k of a token range,
-//                                         block histogram -> row b of the
-//                                         count matrix (workspace)
-//                    route_scatter_kernel G blocks: every block reduces the
-//                                         count matrix (totals and the prefix
-//                                         of earlier blocks), scans the totals
-//                                         into offsets and ranks its own slots
-//   one-block path   route_fused_kernel   all of the above in one block
+//   two-kernel path  route_rank_kernel    G blocks, each a contiguous token
+//                                         range: top-k and weights, the rank of
+//                                         every slot among the block's slots of
+//                                         the same expert (kept in inv_perm),
+//                                         and the block's histogram (row b of
+//                                         the count matrix in the workspace)
+//                    route_place_kernel   G blocks: reduce the count matrix
+//                                         (totals; prefix of earlier blocks),
+//                                         scan the totals into offsets, place
+//                                         each slot at offset + prefix + rank
+//   one-block path   route_fused_kernel   both in one block (small T)
+//
+// Ranking inside a block: warp w owns a contiguous run of the block's tokens
+// and keeps per-expert counters cnt[w][e] in shared memory. In every round a
+// warp finishes the top-k of one token per lane group; lanes holding a pick
+// are in slot order, so __match_any_sync on the expert gives each pick its
+// rank among same-expert picks of the round (the popcount of lower peers),
+// added to cnt[w][e]. After all rounds an exclusive scan over warps turns the
+// counters into per-warp starts, added to every slot's rank.
 #include "moe_device.cuh"
 #include "moe_launch.h"
+#include "rows_common.cuh"
 
 #include <algorithm>
-#include <mutex>
 
 namespace moe {
 namespace {
@@ -30,8 +41,9 @@ namespace {
 struct RouteArgs {
     const float* logits;
     int T, E, k, renorm;
-    int Ep;    // count-matrix row stride
+    int Ep;    // count-matrix row stride (E rounded up to 4)
     int tpc;   // tokens per block
+    int tpw;   // tokens per warp (a multiple of the token groups per warp)
     int G;     // blocks
     int32_t* topk_ids;
     float* topk_weights;
@@ -93,12 +105,11 @@ __device__ __forceinline__ float group_sum(float v) {
 // (the float is recovered exactly from its key). Each of the k rounds takes
 // the group maximum of the keys and, among lanes holding it, the lowest
 // expert index; the owner then drops that expert. Lane j < k keeps the j-th
-// pick and writes it. Every lane of the warp must call (valid may differ
-// between groups of one warp; invalid groups compute on empty keys and write
-// nothing).
+// pick, writes it and its weight, and returns the expert (-1 for lanes
+// without a pick). Every lane of the warp must call (valid may differ between
+// groups of one warp; invalid groups compute on empty keys and write nothing).
 template <int GS, int EPL>
-__device__ __forceinline__ void topk_token(const RouteArgs& a, int t, bool valid, int gl,
-                                           int32_t* s_hist) {
+__device__ __forceinline__ int topk_token(const RouteArgs& a, int t, bool valid, int gl) {
     uint32_t key[EPL];
     const float* row = a.logits + (size_t)t * a.E;
 #pragma unroll
@@ -152,29 +163,59 @@ __device__ __forceinline__ void topk_token(const RouteArgs& a, int t, bool valid
     if (valid && mine) {
         a.topk_ids[(size_t)t * a.k + gl] = my_id;
         a.topk_weights[(size_t)t * a.k + gl] = ej / denom;
-        atomicAdd(&s_hist[my_id], 1);
+        return my_id;
     }
+    return -1;
 }
 
-// Tokens [t0, t1) by a block of NT threads, GS lanes per token; the loop is
-// uniform across each warp so the group reductions see full warps.
+// Top-k of the tokens [t0, t1) and the rank of every slot among this warp's
+// slots of the same expert (written to inv_perm[s]); s_cnt is [NW][E] and
+// counts each warp's picks per expert. Warp w owns tokens
+// [t0 + w*tpw, t0 + (w+1)*tpw); each round takes GPW consecutive tokens, one
+// per lane group, so lane order within a round is slot order.
 template <int GS, int EPL, int NT>
-__device__ __forceinline__ void topk_range(const RouteArgs& a, int t0, int t1, int32_t* s_hist) {
+__device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int t1, int32_t* s_cnt) {
     constexpr int GPW = kWarp / GS;
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
     const int grp = lane / GS;
     const int gl = lane % GS;
-    for (int tb = t0 + warp * GPW; tb < t1; tb += (NT / kWarp) * GPW) {
+    const unsigned lower = (1u << lane) - 1u;
+    int32_t* cnt = s_cnt + (size_t)warp * a.E;
+    const int w0 = t0 + warp * a.tpw;
+    const int w1 = min(t1, w0 + a.tpw);
+    for (int tb = w0; tb < w1; tb += GPW) {
         const int t = tb + grp;
-        topk_token<GS, EPL>(a, t, t < t1, gl, s_hist);
+        const int e = topk_token<GS, EPL>(a, t, t < w1, gl);
+        const unsigned peers = __match_any_sync(kFull, e);
+        if (e >= 0) a.inv_perm[(size_t)t * a.k + gl] = cnt[e] + __popc(peers & lower);
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) cnt[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// Exclusive scan over warps of s_cnt[w][e] for every expert; s_tot[e] gets
+// the block total.
+template <int NT>
+__device__ __forceinline__ void scan_over_warps(int32_t* s_cnt, int32_t* s_tot, int E) {
+    constexpr int NW = NT / kWarp;
+    for (int e = threadIdx.x; e < E; e += NT) {
+        int run = 0;
+#pragma unroll 4
+        for (int w = 0; w < NW; ++w) {
+            const int v = s_cnt[(size_t)w * E + e];
+            s_cnt[(size_t)w * E + e] = run;
+            run += v;
+        }
+        s_tot[e] = run;
     }
 }
 
 // Exclusive scan of in[0..n) into out[0..n) (may alias) by a block of NT
-// threads, n <= MOE_MAX_EXPERTS; returns the total. Uses s_warp[32].
+// threads, n <= MOE_MAX_EXPERTS. Uses s_warp[32].
 template <int NT>
-__device__ int block_exclusive_scan(const int32_t* in, int32_t* out, int n, int32_t* s_warp) {
+__device__ void block_exclusive_scan(const int32_t* in, int32_t* out, int n, int32_t* s_warp) {
     constexpr int ITEMS = (1024 + NT - 1) / NT;
     constexpr int NW = NT / kWarp;
     const int lane = threadIdx.x % kWarp;
@@ -211,110 +252,78 @@ __device__ int block_exclusive_scan(const int32_t* in, int32_t* out, int n, int3
         if (base + i < n) out[base + i] = run;
         run += v[i];
     }
-    const int total = s_warp[NW - 1];
     __syncthreads();
-    return total;
 }
 
-// Stable rank of the slots [s0, s1) inside their experts. s_base[e] is the
-// first row of expert e owned by this block; s_wstart is [NW][E] scratch.
-// The slots are split into one contiguous run per warp (a multiple of 32);
-// pass 1 counts each warp's slots per expert, a scan over warps turns the
-// counts into per-warp starting rows, pass 2 ranks each 32-slot chunk with
-// __match_any_sync (lanes with the same expert) and the popcount of the
-// lower-lane peers, then advances the warp's counter. Slot order decides the
-// rank, so the result is deterministic.
-template <int NT>
-__device__ void scatter_slots(const RouteArgs& a, int s0, int s1, const int32_t* s_base,
-                              int32_t* s_wstart) {
-    constexpr int NW = NT / kWarp;
-    const int lane = threadIdx.x % kWarp;
-    const int warp = threadIdx.x / kWarp;
-    const int E = a.E;
-    const int n = s1 - s0;
-    const int per = (((n + NW - 1) / NW) + kWarp - 1) / kWarp * kWarp;
-    const int lo = s0 + warp * per;
-    const int hi = min(s1, lo + per);
-    int32_t* mine = s_wstart + (size_t)warp * E;
-    const unsigned lower = (1u << lane) - 1u;
-
-    for (int e = lane; e < E; e += kWarp) mine[e] = 0;
-    __syncwarp();
-    for (int c = lo; c < hi; c += kWarp) {
-        const int s = c + lane;
-        const int e = (s < hi) ? __ldcg(a.topk_ids + s) : -1;
-        const unsigned peers = __match_any_sync(kFull, e);
-        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
-        __syncwarp();
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += NT) {
-        int run = s_base[e];
-        for (int w = 0; w < NW; ++w) {
-            const int v = s_wstart[(size_t)w * E + e];
-            s_wstart[(size_t)w * E + e] = run;
-            run += v;
-        }
-    }
-    __syncthreads();
-    for (int c = lo; c < hi; c += kWarp) {
-        const int s = c + lane;
-        const int e = (s < hi) ? __ldcg(a.topk_ids + s) : -1;
-        const unsigned peers = __match_any_sync(kFull, e);
-        if (e >= 0) {
-            const int p = mine[e] + __popc(peers & lower);
+// Add each slot's per-warp start to its within-warp rank for the slots of
+// tokens [t0, t1). With PLACE (one-block path) the expert's offset is added
+// too, the result is final and perm is written.
+template <int NT, bool PLACE>
+__device__ __forceinline__ void finish_ranks(const RouteArgs& a, int t0, int t1, const int32_t* s_cnt,
+                                             const int32_t* s_off) {
+    const int s0 = t0 * a.k, s1 = t1 * a.k;
+    for (int s = s0 + threadIdx.x; s < s1; s += NT) {
+        const int e = __ldcg(a.topk_ids + s);
+        const int w = (s / a.k - t0) / a.tpw;
+        int p = __ldcg(a.inv_perm + s) + s_cnt[(size_t)w * a.E + e];
+        if constexpr (PLACE) {
+            p += s_off[e];
             a.perm[p] = s;
-            a.inv_perm[s] = p;
         }
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
-        __syncwarp();
+        a.inv_perm[s] = p;
     }
 }
 
 template <int GS, int EPL, int NT>
-__global__ void __launch_bounds__(NT) route_topk_kernel(RouteArgs a) {
+__global__ void __launch_bounds__(NT) route_rank_kernel(RouteArgs a) {
+    constexpr int NW = NT / kWarp;
     extern __shared__ int32_t smem[];
-    int32_t* s_hist = smem;  // [Ep]
-    for (int e = threadIdx.x; e < a.Ep; e += NT) s_hist[e] = 0;
+    int32_t* s_cnt = smem;                      // [NW][E]
+    int32_t* s_tot = s_cnt + (size_t)NW * a.E;  // [Ep]
+    pdl_wait_and_release();
+    for (int i = threadIdx.x; i < NW * a.E; i += NT) s_cnt[i] = 0;
+    for (int e = threadIdx.x; e < a.Ep; e += NT) s_tot[e] = 0;
     __syncthreads();
     const int t0 = blockIdx.x * a.tpc;
     const int t1 = min(a.T, t0 + a.tpc);
-    topk_range<GS, EPL, NT>(a, t0, t1, s_hist);
+    topk_rank_range<GS, EPL, NT>(a, t0, t1, s_cnt);
+    __syncthreads();
+    scan_over_warps<NT>(s_cnt, s_tot, a.E);
     __syncthreads();
     int32_t* row = a.ws_counts + (size_t)blockIdx.x * a.Ep;
-    for (int e = threadIdx.x; e < a.Ep; e += NT) row[e] = s_hist[e];
+    for (int e = threadIdx.x; e < a.Ep; e += NT) row[e] = s_tot[e];
+    finish_ranks<NT, false>(a, t0, t1, s_cnt, nullptr);
 }
 
-// Scatter-kernel shared memory, in int32 words.
-__host__ __device__ inline int scatter_rowgroups(int Ep, int nt) {
+// Number of row groups the place kernel splits the count matrix into.
+__host__ __device__ inline int place_rowgroups(int Ep, int nt) {
     const int cg = Ep / 4;
     return cg >= nt ? 1 : nt / cg;
 }
 
 template <int NT>
-__global__ void __launch_bounds__(NT) route_scatter_kernel(RouteArgs a) {
+__global__ void __launch_bounds__(NT) route_place_kernel(RouteArgs a) {
     extern __shared__ int32_t smem[];
     const int Ep = a.Ep;
     const int CG = Ep / 4;
-    const int R = scatter_rowgroups(Ep, NT);
+    const int R = place_rowgroups(Ep, NT);
     int32_t* s_ptot = smem;                 // [R][Ep]
     int32_t* s_ppre = s_ptot + R * Ep;      // [R][Ep]
     int32_t* s_tot = s_ppre + R * Ep;       // [Ep]
     int32_t* s_base = s_tot + Ep;           // [Ep]
     int32_t* s_warp = s_base + Ep;          // [32]
-    int32_t* s_wstart = s_warp + 32;        // [NW][E]
     const int b = blockIdx.x;
+    pdl_wait_and_release();
 
-    // Column sums of the count matrix: all blocks (totals) and blocks before
-    // this one (prefix). Rows are interleaved over R row groups, columns are
-    // read as int4 so each warp reads contiguous 512-byte runs.
+    // Column sums of the count matrix over all blocks (totals) and over the
+    // blocks before this one (prefix). Rows are interleaved over R row
+    // groups; columns are read as int4, contiguous across a warp.
     for (int idx = threadIdx.x; idx < R * CG; idx += NT) {
         const int r = idx / CG;
         const int cg = idx % CG;
         int4 tot = make_int4(0, 0, 0, 0), pre = make_int4(0, 0, 0, 0);
         for (int rb = r; rb < a.G; rb += R) {
-            const int4 v = __ldg(reinterpret_cast<const int4*>(a.ws_counts + (size_t)rb * Ep) + cg);
+            const int4 v = __ldcg(reinterpret_cast<const int4*>(a.ws_counts + (size_t)rb * Ep) + cg);
             tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
             if (rb < b) { pre.x += v.x; pre.y += v.y; pre.z += v.z; pre.w += v.w; }
         }
@@ -340,28 +349,35 @@ __global__ void __launch_bounds__(NT) route_scatter_kernel(RouteArgs a) {
     if (b == 0 && threadIdx.x == 0) a.expert_offsets[a.E] = a.T * a.k;
     __syncthreads();
 
-    const int t0 = b * a.tpc;
-    const int t1 = min(a.T, t0 + a.tpc);
-    scatter_slots<NT>(a, t0 * a.k, t1 * a.k, s_base, s_wstart);
+    const int s0 = b * a.tpc * a.k;
+    const int s1 = min(a.T, (b + 1) * a.tpc) * a.k;
+    for (int s = s0 + threadIdx.x; s < s1; s += NT) {
+        const int e = __ldcg(a.topk_ids + s);
+        const int p = s_base[e] + __ldcg(a.inv_perm + s);
+        a.perm[p] = s;
+        a.inv_perm[s] = p;
+    }
 }
 
 template <int GS, int EPL, int NT>
 __global__ void __launch_bounds__(NT) route_fused_kernel(RouteArgs a) {
+    constexpr int NW = NT / kWarp;
     extern __shared__ int32_t smem[];
-    const int Ep = a.Ep;
-    int32_t* s_hist = smem;            // [Ep] counts, then offsets
-    int32_t* s_warp = s_hist + Ep;     // [32]
-    int32_t* s_wstart = s_warp + 32;   // [NW][E]
-    for (int e = threadIdx.x; e < Ep; e += NT) s_hist[e] = 0;
+    int32_t* s_cnt = smem;                      // [NW][E]
+    int32_t* s_tot = s_cnt + (size_t)NW * a.E;  // [Ep] totals, then offsets
+    int32_t* s_warp = s_tot + a.Ep;             // [32]
+    pdl_wait_and_release();
+    for (int i = threadIdx.x; i < NW * a.E; i += NT) s_cnt[i] = 0;
     __syncthreads();
-    topk_range<GS, EPL, NT>(a, 0, a.T, s_hist);
+    topk_rank_range<GS, EPL, NT>(a, 0, a.T, s_cnt);
     __syncthreads();
-    for (int e = threadIdx.x; e < a.E; e += NT) a.expert_counts[e] = s_hist[e];
-    block_exclusive_scan<NT>(s_hist, s_hist, a.E, s_warp);
-    for (int e = threadIdx.x; e < a.E; e += NT) a.expert_offsets[e] = s_hist[e];
+    scan_over_warps<NT>(s_cnt, s_tot, a.E);
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += NT) a.expert_counts[e] = s_tot[e];
+    block_exclusive_scan<NT>(s_tot, s_tot, a.E, s_warp);
+    for (int e = threadIdx.x; e < a.E; e += NT) a.expert_offsets[e] = s_tot[e];
     if (threadIdx.x == 0) a.expert_offsets[a.E] = a.T * a.k;
-    __syncthreads();
-    scatter_slots<NT>(a, 0, a.T * a.k, s_hist, s_wstart);
+    finish_ranks<NT, true>(a, 0, a.T, s_cnt, s_tot);
 }
 
 constexpr int kNtSplit = 512;
@@ -379,17 +395,15 @@ cudaError_t launch_route_t(const RoutePlan& p, const RouteArgs& a, cudaStream_t 
     if (p.fused) {
         auto kf = route_fused_kernel<GS, EPL, kNtFused>;
         if ((err = allow_smem(kf, p.smem_topk)) != cudaSuccess) return err;
-        kf<<<1, kNtFused, p.smem_topk, stream>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(kf, dim3(1), dim3(kNtFused), p.smem_topk, stream, a);
     }
-    auto k1 = route_topk_kernel<GS, EPL, kNtSplit>;
-    auto k2 = route_scatter_kernel<kNtSplit>;
+    auto k1 = route_rank_kernel<GS, EPL, kNtSplit>;
+    auto k2 = route_place_kernel<kNtSplit>;
     if ((err = allow_smem(k1, p.smem_topk)) != cudaSuccess) return err;
     if ((err = allow_smem(k2, p.smem_scatter)) != cudaSuccess) return err;
-    k1<<<p.G, kNtSplit, p.smem_topk, stream>>>(a);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    k2<<<p.G, kNtSplit, p.smem_scatter, stream>>>(a);
-    return cudaGetLastError();
+    if ((err = launch_pdl(k1, dim3(p.G), dim3(kNtSplit), p.smem_topk, stream, a)) != cudaSuccess)
+        return err;
+    return launch_pdl(k2, dim3(p.G), dim3(kNtSplit), p.smem_scatter, stream, a);
 }
 
 }  // namespace
@@ -402,27 +416,31 @@ RoutePlan plan_route(int64_t T, int E, int k) {
     else { p.gs = 32; p.epl = (E + 31) / 32; }
     if (p.epl > 2) p.epl = p.epl <= 4 ? 4 : p.epl <= 8 ? 8 : p.epl <= 16 ? 16 : 32;
     p.Ep = (E + 3) / 4 * 4;
-    const int fused_groups = (kNtFused / kWarp) * (kWarp / p.gs);
+    const int gpw = kWarp / p.gs;
+    const int fused_groups = (kNtFused / kWarp) * gpw;
     p.fused = T <= 2 * fused_groups;
     if (p.fused) {
+        const int nw = kNtFused / kWarp;
         p.nt = kNtFused;
         p.G = 1;
         p.tpc = int(T);
+        p.tpw = int(((T + nw - 1) / nw + gpw - 1) / gpw * gpw);
         p.ws_bytes = 0;
-        p.smem_topk = sizeof(int32_t) * (size_t(p.Ep) + 32 + size_t(kNtFused / kWarp) * E);
+        p.smem_topk = sizeof(int32_t) * (size_t(nw) * E + p.Ep + 32);
         return p;
     }
+    const int nw = kNtSplit / kWarp;
     p.nt = kNtSplit;
-    const int groups = (kNtSplit / kWarp) * (kWarp / p.gs);
+    const int groups = nw * gpw;
     const int gmax = std::max(1, std::min(128, 32768 / p.Ep));
-    int64_t tpc = std::max<int64_t>(groups, (T + gmax - 1) / gmax);
+    const int64_t tpc = std::max<int64_t>(groups, (T + gmax - 1) / gmax);
     p.tpc = int(tpc);
+    p.tpw = int(((tpc + nw - 1) / nw + gpw - 1) / gpw * gpw);
     p.G = int((T + tpc - 1) / tpc);
     p.ws_bytes = sizeof(int32_t) * size_t(p.G) * size_t(p.Ep);
-    p.smem_topk = sizeof(int32_t) * size_t(p.Ep);
-    const int R = scatter_rowgroups(p.Ep, kNtSplit);
-    p.smem_scatter = sizeof(int32_t) *
-        (size_t(2) * R * p.Ep + 2 * size_t(p.Ep) + 32 + size_t(kNtSplit / kWarp) * E);
+    p.smem_topk = sizeof(int32_t) * (size_t(nw) * E + p.Ep);
+    const int R = place_rowgroups(p.Ep, kNtSplit);
+    p.smem_scatter = sizeof(int32_t) * (size_t(2) * R * p.Ep + 2 * size_t(p.Ep) + 32);
     return p;
 }
 
@@ -433,7 +451,7 @@ cudaError_t launch_route(const RoutePlan& plan, const float* logits, int T, int 
     RouteArgs a;
     a.logits = logits;
     a.T = T; a.E = E; a.k = k; a.renorm = renorm;
-    a.Ep = plan.Ep; a.tpc = plan.tpc; a.G = plan.G;
+    a.Ep = plan.Ep; a.tpc = plan.tpc; a.tpw = plan.tpw; a.G = plan.G;
     a.topk_ids = topk_ids; a.topk_weights = topk_weights;
     a.expert_counts = expert_counts; a.expert_offsets = expert_offsets;
     a.perm = perm; a.inv_perm = inv_perm;

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <utility>
 
 namespace moe {
 
@@ -21,14 +22,44 @@ inline bool can_use_32b(uint64_t row_bytes, std::initializer_list<const void*> p
 // Grid for a grid-stride kernel over `items` work items, each block taking
 // `per_block` items per sweep: never more blocks than the items need, and at
 // most as many as fit on the device at once (every SM busy, one wave).
+// `occ` is the kernel's resident blocks per SM (resident_blocks()).
+#ifndef MOE_GRID_WAVES
+#define MOE_GRID_WAVES 1
+#endif
+inline int grid_for(int occ, uint64_t items, uint64_t per_block, int num_sms) {
+    const uint64_t need = (items + per_block - 1) / per_block;
+    const uint64_t cap = uint64_t(num_sms) * uint64_t(std::max(occ, 1)) * MOE_GRID_WAVES;
+    return int(std::max<uint64_t>(1, std::min(need, cap)));
+}
+
+// Resident blocks per SM of a kernel at block size nt (no dynamic shared
+// memory). The answer depends only on the kernel and the architecture, so
+// callers cache it per kernel instantiation.
 template <typename Kernel>
-inline int grid_for(Kernel kernel, int nt, uint64_t items, uint64_t per_block, int num_sms) {
+inline int resident_blocks(Kernel kernel, int nt) {
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, nt, 0) != cudaSuccess || occ < 1)
         occ = 1;
-    const uint64_t need = (items + per_block - 1) / per_block;
-    const uint64_t cap = uint64_t(num_sms) * uint64_t(occ);
-    return int(std::max<uint64_t>(1, std::min(need, cap)));
+    return occ;
+}
+
+// Launch with programmatic stream serialisation (see pdl_wait_and_release):
+// the kernel may be scheduled before the previous kernel on the stream ends
+// and must call pdl_wait_and_release() before its first global access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Work items per launch stay below 2^31 so 32-bit grid-stride indices never

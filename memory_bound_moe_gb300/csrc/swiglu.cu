@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(NT) swiglu_kernel(const uint8_t* __restrict__ 
                                                     uint8_t* __restrict__ act, uint32_t total,
                                                     DivU32 nv, uint32_t in_row_bytes,
                                                     uint32_t out_row_bytes) {
+    pdl_wait_and_release();
     const uint32_t stride = gridDim.x * NT * U;
     for (uint32_t base = blockIdx.x * NT * U + threadIdx.x; base < total; base += stride) {
         Bits<VB> g[U], u[U];
@@ -66,24 +67,31 @@ __global__ void __launch_bounds__(NT) swiglu_kernel(const uint8_t* __restrict__ 
     }
 }
 
-constexpr int kNt = 256;
-constexpr int kUnroll = 2;
+#ifndef MOE_SWIGLU_NT
+#define MOE_SWIGLU_NT 256
+#endif
+#ifndef MOE_SWIGLU_UNROLL
+#define MOE_SWIGLU_UNROLL 2
+#endif
+constexpr int kNt = MOE_SWIGLU_NT;
+constexpr int kUnroll = MOE_SWIGLU_UNROLL;
 
 template <int VB>
 cudaError_t launch_vb(const uint16_t* gate_up, int64_t rows, int I, uint16_t* act, int num_sms,
                       cudaStream_t stream) {
     auto kernel = swiglu_kernel<VB, kUnroll, kNt>;
+    static const int occ = resident_blocks(kernel, kNt);
     const uint32_t nv = uint32_t(uint64_t(I) * 2 / VB);
     const int64_t rows_per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / nv));
     for (int64_t r0 = 0; r0 < rows; r0 += rows_per_launch) {
         const int64_t nr = std::min(rows_per_launch, rows - r0);
         const uint32_t total = uint32_t(nr * nv);
-        const int grid = grid_for(kernel, kNt, total, uint64_t(kNt) * kUnroll, num_sms);
-        kernel<<<grid, kNt, 0, stream>>>(
+        const int grid = grid_for(occ, total, uint64_t(kNt) * kUnroll, num_sms);
+        const cudaError_t err = launch_pdl(
+            kernel, dim3(grid), dim3(kNt), 0, stream,
             reinterpret_cast<const uint8_t*>(gate_up + r0 * 2 * int64_t(I)),
             reinterpret_cast<uint8_t*>(act + r0 * int64_t(I)), total, DivU32::make(nv),
             uint32_t(4 * int64_t(I)), uint32_t(2 * int64_t(I)));
-        const cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
