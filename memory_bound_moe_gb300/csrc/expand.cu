@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(NT) expand_kernel(const uint8_t* __restrict__ 
 #define MOE_EXPAND_NT 256
 #endif
 #ifndef MOE_EXPAND_UNROLL
-#define MOE_EXPAND_UNROLL 2
+#define MOE_EXPAND_UNROLL 1
 #endif
 constexpr int kNt = MOE_EXPAND_NT;
 constexpr int kUnroll = MOE_EXPAND_UNROLL;

@@ -100,24 +100,29 @@ __device__ __forceinline__ float group_sum(float v) {
     return v;
 }
 
-// Top-k of one token by a group of GS lanes; lane gl holds experts
-// gl, gl + GS, gl + 2GS, ... (coalesced row read) as order-preserving keys
-// (the float is recovered exactly from its key). Each of the k rounds takes
-// the group maximum of the keys and, among lanes holding it, the lowest
-// expert index; the owner then drops that expert. Lane j < k keeps the j-th
-// pick, writes it and its weight, and returns the expert (-1 for lanes
-// without a pick). Every lane of the warp must call (valid may differ between
-// groups of one warp; invalid groups compute on empty keys and write nothing).
+// Keys of token t for lane gl of a GS-lane group: experts gl, gl + GS, ...
+// (a coalesced row read) as order-preserving keys; 0 outside the row.
 template <int GS, int EPL>
-__device__ __forceinline__ int topk_token(const RouteArgs& a, int t, bool valid, int gl) {
-    uint32_t key[EPL];
+__device__ __forceinline__ void load_keys(const RouteArgs& a, int t, bool valid, int gl,
+                                          uint32_t (&key)[EPL]) {
     const float* row = a.logits + (size_t)t * a.E;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
         const int e = gl + GS * i;
         key[i] = (valid && e < a.E) ? order_key(__ldg(row + e)) : 0u;
     }
+}
 
+// Top-k of one token by a group of GS lanes from its keys (the float is
+// recovered exactly from its key). Each of the k rounds takes the group
+// maximum of the keys and, among lanes holding it, the lowest expert index;
+// the owner then drops that expert. Lane j < k keeps the j-th pick, writes it
+// and its weight, and returns the expert (-1 for lanes without a pick). Every
+// lane of the warp must call (valid may differ between groups of one warp;
+// invalid groups compute on empty keys and write nothing).
+template <int GS, int EPL>
+__device__ __forceinline__ int topk_select(const RouteArgs& a, int t, bool valid, int gl,
+                                           uint32_t (&key)[EPL]) {
     // Softmax denominator over all E experts (only without renormalisation),
     // taken before the picks remove keys.
     float z = 0.0f;
@@ -168,13 +173,21 @@ __device__ __forceinline__ int topk_token(const RouteArgs& a, int t, bool valid,
     return -1;
 }
 
+// Rounds whose (expert, rank) per lane stay in registers until the ranks are
+// finished; later rounds (only for very long token runs) go through inv_perm.
+constexpr int kRegRounds = 4;
+
 // Top-k of the tokens [t0, t1) and the rank of every slot among this warp's
-// slots of the same expert (written to inv_perm[s]); s_cnt is [NW][E] and
-// counts each warp's picks per expert. Warp w owns tokens
-// [t0 + w*tpw, t0 + (w+1)*tpw); each round takes GPW consecutive tokens, one
-// per lane group, so lane order within a round is slot order.
+// slots of the same expert; s_cnt is [NW][E] and counts each warp's picks per
+// expert. Warp w owns tokens [t0 + w*tpw, t0 + (w+1)*tpw); each round takes
+// GPW consecutive tokens, one per lane group, so lane order within a round
+// is slot order. The first kRegRounds rounds return each lane's expert and
+// rank in re/rr (expert -1: no slot); the rank of later rounds is written to
+// inv_perm[s]. The next round's logits are loaded before the current round's
+// selection.
 template <int GS, int EPL, int NT>
-__device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int t1, int32_t* s_cnt) {
+__device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int t1, int32_t* s_cnt,
+                                                int (&re)[kRegRounds], int (&rr)[kRegRounds]) {
     constexpr int GPW = kWarp / GS;
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
@@ -184,9 +197,34 @@ __device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int 
     int32_t* cnt = s_cnt + (size_t)warp * a.E;
     const int w0 = t0 + warp * a.tpw;
     const int w1 = min(t1, w0 + a.tpw);
-    for (int tb = w0; tb < w1; tb += GPW) {
+
+    uint32_t key[EPL], next[EPL];
+    load_keys<GS, EPL>(a, w0 + grp, w0 + grp < w1, gl, key);
+#pragma unroll
+    for (int r = 0; r < kRegRounds; ++r) {
+        re[r] = -1;
+        rr[r] = 0;
+        const int tb = w0 + r * GPW;
+        if (tb < w1) {
+            const int tn = tb + GPW + grp;
+            load_keys<GS, EPL>(a, tn, tn < w1, gl, next);
+            const int t = tb + grp;
+            const int e = topk_select<GS, EPL>(a, t, t < w1, gl, key);
+            const unsigned peers = __match_any_sync(kFull, e);
+            re[r] = e;
+            rr[r] = (e >= 0) ? cnt[e] + __popc(peers & lower) : 0;
+            __syncwarp();
+            if (e >= 0 && lane == __ffs(peers) - 1) cnt[e] += __popc(peers);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) key[i] = next[i];
+        }
+    }
+    for (int tb = w0 + kRegRounds * GPW; tb < w1; tb += GPW) {
         const int t = tb + grp;
-        const int e = topk_token<GS, EPL>(a, t, t < w1, gl);
+        const int e = topk_select<GS, EPL>(a, t, t < w1, gl, key);
+        const int tn = tb + GPW + grp;
+        load_keys<GS, EPL>(a, tn, tn < w1, gl, key);
         const unsigned peers = __match_any_sync(kFull, e);
         if (e >= 0) a.inv_perm[(size_t)t * a.k + gl] = cnt[e] + __popc(peers & lower);
         __syncwarp();
@@ -255,17 +293,38 @@ __device__ void block_exclusive_scan(const int32_t* in, int32_t* out, int n, int
     __syncthreads();
 }
 
-// Add each slot's per-warp start to its within-warp rank for the slots of
-// tokens [t0, t1). With PLACE (one-block path) the expert's offset is added
-// too, the result is final and perm is written.
-template <int NT, bool PLACE>
+// Add each slot's per-warp start to its within-warp rank (s_cnt now holds
+// the exclusive scan over warps). With PLACE (one-block path) the expert's
+// offset is added too, the result is final and perm is written.
+template <int GS, int NT, bool PLACE>
 __device__ __forceinline__ void finish_ranks(const RouteArgs& a, int t0, int t1, const int32_t* s_cnt,
-                                             const int32_t* s_off) {
-    const int s0 = t0 * a.k, s1 = t1 * a.k;
-    for (int s = s0 + threadIdx.x; s < s1; s += NT) {
+                                             const int32_t* s_off, const int (&re)[kRegRounds],
+                                             const int (&rr)[kRegRounds]) {
+    constexpr int GPW = kWarp / GS;
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    const int grp = lane / GS;
+    const int gl = lane % GS;
+    const int32_t* start = s_cnt + (size_t)warp * a.E;
+    const int w0 = t0 + warp * a.tpw;
+    const int w1 = min(t1, w0 + a.tpw);
+#pragma unroll
+    for (int r = 0; r < kRegRounds; ++r) {
+        if (re[r] >= 0) {
+            const int s = (w0 + r * GPW + grp) * a.k + gl;
+            int p = rr[r] + start[re[r]];
+            if constexpr (PLACE) {
+                p += s_off[re[r]];
+                a.perm[p] = s;
+            }
+            a.inv_perm[s] = p;
+        }
+    }
+    // slots of rounds past kRegRounds: the rank was kept in inv_perm
+    const int s_lo = (w0 + kRegRounds * GPW) * a.k;
+    for (int s = s_lo + lane; s < w1 * a.k; s += kWarp) {
         const int e = __ldcg(a.topk_ids + s);
-        const int w = (s / a.k - t0) / a.tpw;
-        int p = __ldcg(a.inv_perm + s) + s_cnt[(size_t)w * a.E + e];
+        int p = __ldcg(a.inv_perm + s) + start[e];
         if constexpr (PLACE) {
             p += s_off[e];
             a.perm[p] = s;
@@ -286,13 +345,14 @@ __global__ void __launch_bounds__(NT) route_rank_kernel(RouteArgs a) {
     __syncthreads();
     const int t0 = blockIdx.x * a.tpc;
     const int t1 = min(a.T, t0 + a.tpc);
-    topk_rank_range<GS, EPL, NT>(a, t0, t1, s_cnt);
+    int re[kRegRounds], rr[kRegRounds];
+    topk_rank_range<GS, EPL, NT>(a, t0, t1, s_cnt, re, rr);
     __syncthreads();
     scan_over_warps<NT>(s_cnt, s_tot, a.E);
     __syncthreads();
     int32_t* row = a.ws_counts + (size_t)blockIdx.x * a.Ep;
     for (int e = threadIdx.x; e < a.Ep; e += NT) row[e] = s_tot[e];
-    finish_ranks<NT, false>(a, t0, t1, s_cnt, nullptr);
+    finish_ranks<GS, NT, false>(a, t0, t1, s_cnt, nullptr, re, rr);
 }
 
 // Number of row groups the place kernel splits the count matrix into.
@@ -322,10 +382,20 @@ __global__ void __launch_bounds__(NT) route_place_kernel(RouteArgs a) {
         const int r = idx / CG;
         const int cg = idx % CG;
         int4 tot = make_int4(0, 0, 0, 0), pre = make_int4(0, 0, 0, 0);
-        for (int rb = r; rb < a.G; rb += R) {
-            const int4 v = __ldcg(reinterpret_cast<const int4*>(a.ws_counts + (size_t)rb * Ep) + cg);
-            tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
-            if (rb < b) { pre.x += v.x; pre.y += v.y; pre.z += v.z; pre.w += v.w; }
+        const int4* col = reinterpret_cast<const int4*>(a.ws_counts) + cg;
+        const int q = Ep / 4;   // int4 per row
+        for (int rb0 = r; rb0 < a.G; rb0 += 8 * R) {
+            int4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {   // 8 independent loads in flight
+                const int rb = rb0 + u * R;
+                v[u] = rb < a.G ? __ldcg(col + (size_t)rb * q) : make_int4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                tot.x += v[u].x; tot.y += v[u].y; tot.z += v[u].z; tot.w += v[u].w;
+                if (rb0 + u * R < b) { pre.x += v[u].x; pre.y += v[u].y; pre.z += v[u].z; pre.w += v[u].w; }
+            }
         }
         reinterpret_cast<int4*>(s_ptot + r * Ep)[cg] = tot;
         reinterpret_cast<int4*>(s_ppre + r * Ep)[cg] = pre;
@@ -369,7 +439,8 @@ __global__ void __launch_bounds__(NT) route_fused_kernel(RouteArgs a) {
     pdl_wait_and_release();
     for (int i = threadIdx.x; i < NW * a.E; i += NT) s_cnt[i] = 0;
     __syncthreads();
-    topk_rank_range<GS, EPL, NT>(a, 0, a.T, s_cnt);
+    int re[kRegRounds], rr[kRegRounds];
+    topk_rank_range<GS, EPL, NT>(a, 0, a.T, s_cnt, re, rr);
     __syncthreads();
     scan_over_warps<NT>(s_cnt, s_tot, a.E);
     __syncthreads();
@@ -377,11 +448,20 @@ __global__ void __launch_bounds__(NT) route_fused_kernel(RouteArgs a) {
     block_exclusive_scan<NT>(s_tot, s_tot, a.E, s_warp);
     for (int e = threadIdx.x; e < a.E; e += NT) a.expert_offsets[e] = s_tot[e];
     if (threadIdx.x == 0) a.expert_offsets[a.E] = a.T * a.k;
-    finish_ranks<NT, true>(a, 0, a.T, s_cnt, s_tot);
+    finish_ranks<GS, NT, true>(a, 0, a.T, s_cnt, s_tot, re, rr);
 }
 
-constexpr int kNtSplit = 512;
-constexpr int kNtFused = 1024;
+#ifndef MOE_ROUTE_NT
+#define MOE_ROUTE_NT 512
+#endif
+#ifndef MOE_ROUTE_FUSED_NT
+#define MOE_ROUTE_FUSED_NT 512
+#endif
+#ifndef MOE_ROUTE_GMAX
+#define MOE_ROUTE_GMAX 128
+#endif
+constexpr int kNtSplit = MOE_ROUTE_NT;
+constexpr int kNtFused = MOE_ROUTE_FUSED_NT;
 
 template <typename K>
 cudaError_t allow_smem(K kernel, size_t bytes) {
@@ -432,7 +512,7 @@ RoutePlan plan_route(int64_t T, int E, int k) {
     const int nw = kNtSplit / kWarp;
     p.nt = kNtSplit;
     const int groups = nw * gpw;
-    const int gmax = std::max(1, std::min(128, 32768 / p.Ep));
+    const int gmax = std::max(1, std::min(MOE_ROUTE_GMAX, 32768 / p.Ep));
     const int64_t tpc = std::max<int64_t>(groups, (T + gmax - 1) / gmax);
     p.tpc = int(tpc);
     p.tpw = int(((tpc + nw - 1) / nw + gpw - 1) / gpw * gpw);

@@ -24,7 +24,7 @@ inline bool can_use_32b(uint64_t row_bytes, std::initializer_list<const void*> p
 // most as many as fit on the device at once (every SM busy, one wave).
 // `occ` is the kernel's resident blocks per SM (resident_blocks()).
 #ifndef MOE_GRID_WAVES
-#define MOE_GRID_WAVES 1
+#define MOE_GRID_WAVES 4
 #endif
 inline int grid_for(int occ, uint64_t items, uint64_t per_block, int num_sms) {
     const uint64_t need = (items + per_block - 1) / per_block;

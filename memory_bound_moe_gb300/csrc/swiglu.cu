@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(NT) swiglu_kernel(const uint8_t* __restrict__ 
 #define MOE_SWIGLU_NT 256
 #endif
 #ifndef MOE_SWIGLU_UNROLL
-#define MOE_SWIGLU_UNROLL 2
+#define MOE_SWIGLU_UNROLL 1
 #endif
 constexpr int kNt = MOE_SWIGLU_NT;
 constexpr int kUnroll = MOE_SWIGLU_UNROLL;
