@@ -396,6 +396,80 @@ def time_e2e(w, inputs, steps, warmup, dev, n_copy_streams=4, chunk_bytes=32 << 
     return ms, h2d, d2h_bytes
 
 
+def decode_latency(dev, reps=2000):
+    """Latency of one MoE-layer pass on the decode workload (T=16, H=7168,
+    E=256, top-8, I=2048): the four calls (route, expand, SwiGLU, combine)
+    and the three calls with routing and expansion in one launch
+    (moe_route_expand), each issued back to back through direct C-ABI calls
+    and replayed from a CUDA graph captured once. Per-layer time = elapsed
+    time over `reps` passes / reps."""
+    import torch
+    import memory_bound_moe_gb300 as moe
+    from memory_bound_moe_gb300.workloads import WORKLOADS, generate
+    lib = moe.load_library()
+    w = WORKLOADS["decode"]
+    inp = {kk: v.to(dev) for kk, v in generate(w, seed=0).items()}
+    T, E, k, S, H, I = w.T, w.E, w.k, w.S, w.H, w.I
+    i32 = dict(dtype=torch.int32, device=dev)
+    ids = torch.empty((T, k), **i32)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+    cnt = torch.empty((E,), **i32)
+    off = torch.empty((E + 1,), **i32)
+    perm = torch.empty((S,), **i32)
+    inv = torch.empty((S,), **i32)
+    ex = torch.empty((S, H), dtype=torch.bfloat16, device=dev)
+    act = torch.empty((S, I), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    p = lambda t: t.data_ptr()
+    rn = int(w.renorm)
+
+    def four(sp):
+        st = lib.moe_route(p(inp["logits"]), T, E, k, rn, p(ids), p(wts), p(cnt), p(off), p(perm),
+                           p(inv), 0, 0, sp)
+        st |= lib.moe_expand(p(inp["x"]), T, H, k, p(inv), p(ex), sp)
+        st |= lib.moe_swiglu(p(inp["gate_up"]), S, I, p(act), sp)
+        st |= lib.moe_combine(p(inp["expert_out"]), T, H, k, p(wts), p(inv), p(out), sp)
+        assert st == 0
+
+    def three(sp):
+        st = lib.moe_route_expand(p(inp["logits"]), T, E, k, rn, p(inp["x"]), H, p(ids), p(wts),
+                                  p(cnt), p(off), p(perm), p(inv), p(ex), 0, 0, sp)
+        st |= lib.moe_swiglu(p(inp["gate_up"]), S, I, p(act), sp)
+        st |= lib.moe_combine(p(inp["expert_out"]), T, H, k, p(wts), p(inv), p(out), sp)
+        assert st == 0
+
+    def timed(fn):
+        sp = torch.cuda.current_stream(dev).cuda_stream
+        for _ in range(20):
+            fn(sp)
+        torch.cuda.synchronize(dev)
+        torch.cuda._sleep(8_000_000)     # let the host enqueue ahead of the GPU
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn(sp)
+        b.record()
+        torch.cuda.synchronize(dev)
+        return 1e3 * a.elapsed_time(b) / reps
+
+    def graphed(fn):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            fn(side.cuda_stream)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(torch.cuda.current_stream(dev).cuda_stream)
+        return lambda sp: g.replay()
+
+    res = {"four_calls_stream_us": timed(four), "route_expand_stream_us": timed(three),
+           "four_calls_graph_us": timed(graphed(four)), "route_expand_graph_us": timed(graphed(three)),
+           "workload": w.describe()}
+    return {kk: (round(v, 3) if isinstance(v, float) else v) for kk, v in res.items()}
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
@@ -582,6 +656,8 @@ def main():
                       "double-buffered device sets; the C-ABI calls through the Python binding; "
                       "out copied back on a separate stream"}
 
+    decode = decode_latency(dev) if args.workload == WORKLOAD else None
+
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         cpu = cpu_baseline(w, inputs, args.cpu_budget)
@@ -593,6 +669,7 @@ def main():
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_dict(w),
             "roofline": roofline, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": step.launches_per_step * args.steps,
+            "decode_latency": decode,
             "clocks": clk, "remeasured": remeasured, "wall_s_timed_region": round(wall, 3),
             "device": torch.cuda.get_device_name(dev),
         }

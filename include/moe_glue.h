@@ -126,6 +126,30 @@ moe_status_t moe_route(const float* logits, int64_t T, int E, int k, int renorm,
                        moe_stream_t stream);
 
 /*
+ * Routing and row expansion as one call: the same outputs as moe_route
+ * followed by moe_expand (bit-identical), with the argument rules of both.
+ * "CuTeDSL at Perplexity", section "Mixture of Experts (MoE) dispatch/combine",
+ * sub-section "Local", and section "Grid synchronization": for decode-sized
+ * batches the pages fuse routing and token copy into one launch and choose
+ * between that and separate route + copy kernels on the host.
+ *
+ * When moe_route_workspace_size(T, E, k) is 0 (decode-sized T: at most 32
+ * tokens for E > 16, 64 for E <= 16, 128 for E <= 8) this is ONE kernel
+ * launch: every block routes the whole batch in shared memory (block 0
+ * writes the routing outputs) and copies its share of the rows, with no
+ * grid-wide synchronisation. Otherwise it launches the moe_route kernels and
+ * then the moe_expand kernel on the same stream, and `workspace` must be as
+ * for moe_route.
+ */
+moe_status_t moe_route_expand(const float* logits, int64_t T, int E, int k, int renorm,
+                              const moe_bf16_t* x, int H,
+                              int32_t* topk_ids, float* topk_weights,
+                              int32_t* expert_counts, int32_t* expert_offsets,
+                              int32_t* perm, int32_t* inv_perm, moe_bf16_t* expanded_x,
+                              void* workspace, size_t workspace_bytes,
+                              moe_stream_t stream);
+
+/*
  * moe_route without a caller-provided workspace: the same computation,
  * outputs, validation and status codes as moe_route, with the routing
  * scratch held in a device array inside the library. The pages have no

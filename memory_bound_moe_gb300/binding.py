@@ -57,6 +57,9 @@ def load_library():
         lib.moe_route.argtypes = [_vp, _i64, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp,
                                   _vp, ctypes.c_size_t, _vp]
         lib.moe_route.restype = _int
+        lib.moe_route_expand.argtypes = [_vp, _i64, _int, _int, _int, _vp, _int, _vp, _vp, _vp,
+                                         _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        lib.moe_route_expand.restype = _int
         lib.moe_expand.argtypes = [_vp, _i64, _int, _int, _vp, _vp, _vp]
         lib.moe_expand.restype = _int
         lib.moe_swiglu.argtypes = [_vp, _i64, _int, _vp, _vp]
@@ -150,6 +153,52 @@ def moe_route(logits: torch.Tensor, k: int, renorm: bool, *, out: Optional[Route
                                   _stream_ptr(stream, dev))
     _check("moe_route", st)
     return out
+
+
+def _route_outputs(T: int, E: int, k: int, dev) -> RouteResult:
+    i32 = dict(dtype=torch.int32, device=dev)
+    return RouteResult(torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev),
+                       torch.empty((E,), **i32), torch.empty((E + 1,), **i32),
+                       torch.empty((T * k,), **i32), torch.empty((T * k,), **i32))
+
+
+def moe_route_expand(logits: torch.Tensor, x: torch.Tensor, k: int, renorm: bool, *,
+                     out: Optional[RouteResult] = None, expanded: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None):
+    """Routing of ``logits [T, E]`` and expansion of ``x [T, H]`` in one call
+    (one kernel launch for decode-sized T). Returns ``(RouteResult,
+    expanded_x)``, identical to ``moe_route`` followed by ``moe_expand``."""
+    if logits.dim() != 2 or x.dim() != 2:
+        raise ValueError("logits must be [T, E] and x [T, H]")
+    T, E = logits.shape
+    H = x.shape[1]
+    _need(logits, "logits", torch.float32, (T, E))
+    _need(x, "x", torch.bfloat16, (T, H))
+    dev = logits.device
+    if out is None:
+        out = _route_outputs(T, E, k, dev)
+    if expanded is None:
+        expanded = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+    _need(expanded, "expanded_x", torch.bfloat16, (T * k, H))
+    for name, t, dt, shape in (("topk_ids", out.topk_ids, torch.int32, (T, k)),
+                               ("topk_weights", out.topk_weights, torch.float32, (T, k)),
+                               ("expert_counts", out.expert_counts, torch.int32, (E,)),
+                               ("expert_offsets", out.expert_offsets, torch.int32, (E + 1,)),
+                               ("perm", out.perm, torch.int32, (T * k,)),
+                               ("inv_perm", out.inv_perm, torch.int32, (T * k,))):
+        _need(t, name, dt, shape)
+    ws_bytes = moe_route_workspace_size(T, E, k)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
+    ws_len = 0 if workspace is None else workspace.numel()
+    st = load_library().moe_route_expand(_ptr(logits), T, E, int(k), int(bool(renorm)), _ptr(x), H,
+                                         _ptr(out.topk_ids), _ptr(out.topk_weights),
+                                         _ptr(out.expert_counts), _ptr(out.expert_offsets),
+                                         _ptr(out.perm), _ptr(out.inv_perm), _ptr(expanded),
+                                         _ptr(workspace), ws_len, _stream_ptr(stream, dev))
+    _check("moe_route_expand", st)
+    return out, expanded
 
 
 def moe_expand(x: torch.Tensor, inv_perm: torch.Tensor, k: int, *,

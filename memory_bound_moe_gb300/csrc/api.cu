@@ -138,6 +138,59 @@ moe_status_t moe_route(const float* logits, int64_t T, int E, int k, int renorm,
                                        workspace, s));
 }
 
+moe_status_t moe_route_expand(const float* logits, int64_t T, int E, int k, int renorm,
+                              const moe_bf16_t* x, int H, int32_t* topk_ids, float* topk_weights,
+                              int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
+                              int32_t* inv_perm, moe_bf16_t* expanded_x, void* workspace,
+                              size_t workspace_bytes, moe_stream_t stream) {
+    moe_status_t st = check_route_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(T, H, k)) != MOE_OK) return st;
+    if (T > 0) {
+        if (x == nullptr || expanded_x == nullptr) return MOE_ERR_INVALID_ARG;
+        if (!aligned16(x) || !aligned16(expanded_x)) return MOE_ERR_MISALIGNED;
+        const uint64_t S = uint64_t(T) * uint64_t(k);
+        const uint64_t ws = moe::plan_route(T, E, k).ws_bytes;
+        // expanded_x against every other buffer of the call
+        if (any_overlap({{expanded_x, 2 * S * uint64_t(H)}},
+                        {{x, 2 * uint64_t(T) * uint64_t(H)}, {logits, 4ull * uint64_t(T) * E},
+                         {topk_ids, 4 * S}, {topk_weights, 4 * S}, {expert_counts, 4ull * E},
+                         {expert_offsets, 4ull * (E + 1)}, {perm, 4 * S}, {inv_perm, 4 * S},
+                         {workspace, ws}}))
+            return MOE_ERR_INVALID_ARG;
+        // x is an input of the expansion: no routing output may overlap it
+        if (any_overlap({{x, 2 * uint64_t(T) * uint64_t(H)}},
+                        {{topk_ids, 4 * S}, {topk_weights, 4 * S}, {expert_counts, 4ull * E},
+                         {expert_offsets, 4ull * (E + 1)}, {perm, 4 * S}, {inv_perm, 4 * S},
+                         {workspace, ws}}))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const moe::RoutePlan plan = moe::plan_route(T, E, k);
+    if (T > 0 && moe::route_expand_fits(plan)) {
+        // validate the routing arguments exactly as moe_route does
+        if (expert_counts == nullptr || expert_offsets == nullptr || logits == nullptr ||
+            topk_ids == nullptr || topk_weights == nullptr || perm == nullptr || inv_perm == nullptr)
+            return MOE_ERR_INVALID_ARG;
+        if (!aligned4(expert_counts) || !aligned4(expert_offsets) || !aligned4(logits) ||
+            !aligned4(topk_ids) || !aligned4(topk_weights) || !aligned4(perm) || !aligned4(inv_perm))
+            return MOE_ERR_MISALIGNED;
+        const uint64_t S = uint64_t(T) * uint64_t(k);
+        if (any_overlap({{topk_ids, 4 * S}, {topk_weights, 4 * S}, {expert_counts, 4ull * E},
+                         {expert_offsets, 4ull * (E + 1)}, {perm, 4 * S}, {inv_perm, 4 * S}},
+                        {{logits, 4ull * uint64_t(T) * E}}))
+            return MOE_ERR_INVALID_ARG;
+        int sms = 0;
+        if (current_sm_count(&sms) != cudaSuccess) return MOE_ERR_CUDA;
+        return from_cuda(moe::launch_route_expand(
+            plan, logits, int(T), E, k, renorm ? 1 : 0, topk_ids, topk_weights, expert_counts,
+            expert_offsets, perm, inv_perm, x, H, expanded_x, sms, reinterpret_cast<cudaStream_t>(stream)));
+    }
+    st = moe_route(logits, T, E, k, renorm, topk_ids, topk_weights, expert_counts, expert_offsets,
+                   perm, inv_perm, workspace, workspace_bytes, stream);
+    if (st != MOE_OK || T == 0) return st;
+    return moe_expand(x, T, H, k, inv_perm, expanded_x, stream);
+}
+
 moe_status_t moe_expand(const moe_bf16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
                         moe_bf16_t* expanded_x, moe_stream_t stream) {
     if (k < 1) return MOE_ERR_INVALID_ARG;

@@ -31,6 +31,14 @@ cudaError_t launch_route(const RoutePlan& plan, const float* logits, int T, int 
                          int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
                          int32_t* inv_perm, void* workspace, cudaStream_t stream);
 
+// One-launch route + expand for decode-sized batches (route_expand.cu).
+bool route_expand_fits(const RoutePlan& plan);
+cudaError_t launch_route_expand(const RoutePlan& plan, const float* logits, int T, int E, int k,
+                                int renorm, int32_t* topk_ids, float* topk_weights,
+                                int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
+                                int32_t* inv_perm, const uint16_t* x, int H, uint16_t* expanded_x,
+                                int num_sms, cudaStream_t stream);
+
 cudaError_t launch_expand(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
                           uint16_t* expanded_x, int num_sms, cudaStream_t stream);
 

@@ -31,307 +31,13 @@
 // counters into per-warp starts, added to every slot's rank.
 #include "moe_device.cuh"
 #include "moe_launch.h"
+#include "route_device.cuh"
 #include "rows_common.cuh"
 
 #include <algorithm>
 
 namespace moe {
 namespace {
-
-struct RouteArgs {
-    const float* logits;
-    int T, E, k, renorm;
-    int Ep;    // count-matrix row stride (E rounded up to 4)
-    int tpc;   // tokens per block
-    int tpw;   // tokens per warp (a multiple of the token groups per warp)
-    int G;     // blocks
-    int32_t* topk_ids;
-    float* topk_weights;
-    int32_t* expert_counts;
-    int32_t* expert_offsets;
-    int32_t* perm;
-    int32_t* inv_perm;
-    int32_t* ws_counts;  // [G][Ep]
-};
-
-// Order-preserving map of a float onto uint32 (larger float -> larger key).
-// -0.0 is first folded onto +0.0 so that the two compare equal. Key 0 marks
-// "empty / already taken"; every real logit maps to 1 or more (only one NaN
-// bit pattern would map to 0, and it is lifted to 1), so a pick is always a
-// valid expert.
-__device__ __forceinline__ uint32_t order_key(float v) {
-    v = (v == 0.0f) ? 0.0f : v;
-    const uint32_t b = __float_as_uint(v);
-    return max((b & 0x80000000u) ? ~b : (b | 0x80000000u), 1u);
-}
-
-__device__ __forceinline__ float key_value(uint32_t key) {
-    uint32_t b = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
-    return __uint_as_float(b);
-}
-
-// Reductions over aligned groups of GS lanes; every lane of the warp calls.
-template <int GS>
-__device__ __forceinline__ uint32_t group_max(uint32_t v) {
-    if constexpr (GS == 32) {
-        return __reduce_max_sync(kFull, v);
-    } else {
-#pragma unroll
-        for (int o = GS / 2; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
-        return v;
-    }
-}
-
-template <int GS>
-__device__ __forceinline__ uint32_t group_min(uint32_t v) {
-    if constexpr (GS == 32) {
-        return __reduce_min_sync(kFull, v);
-    } else {
-#pragma unroll
-        for (int o = GS / 2; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(kFull, v, o));
-        return v;
-    }
-}
-
-template <int GS>
-__device__ __forceinline__ float group_sum(float v) {
-#pragma unroll
-    for (int o = GS / 2; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
-}
-
-// Keys of token t for lane gl of a GS-lane group: experts gl, gl + GS, ...
-// (a coalesced row read) as order-preserving keys; 0 outside the row.
-template <int GS, int EPL>
-__device__ __forceinline__ void load_keys(const RouteArgs& a, int t, bool valid, int gl,
-                                          uint32_t (&key)[EPL]) {
-    const float* row = a.logits + (size_t)t * a.E;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        const int e = gl + GS * i;
-        key[i] = (valid && e < a.E) ? order_key(__ldg(row + e)) : 0u;
-    }
-}
-
-// Top-k of one token by a group of GS lanes from its keys (the float is
-// recovered exactly from its key). Each of the k rounds takes the group
-// maximum of the keys and, among lanes holding it, the lowest expert index;
-// the owner then drops that expert. Lane j < k keeps the j-th pick, writes it
-// and its weight, and returns the expert (-1 for lanes without a pick). Every
-// lane of the warp must call (valid may differ between groups of one warp;
-// invalid groups compute on empty keys and write nothing).
-template <int GS, int EPL>
-__device__ __forceinline__ int topk_select(const RouteArgs& a, int t, bool valid, int gl,
-                                           uint32_t (&key)[EPL]) {
-    // Softmax denominator over all E experts (only without renormalisation),
-    // taken before the picks remove keys.
-    float z = 0.0f;
-    if (!a.renorm) {
-        uint32_t lmax = key[0];
-#pragma unroll
-        for (int i = 1; i < EPL; ++i) lmax = max(lmax, key[i]);
-        const float vmax = key_value(group_max<GS>(lmax));
-#pragma unroll
-        for (int i = 0; i < EPL; ++i)
-            if (key[i] != 0u) z += expf(key_value(key[i]) - vmax);
-        z = group_sum<GS>(z);
-    }
-
-    int my_id = 0;
-    float my_val = 0.0f;
-    float vmax = 0.0f;
-    for (int j = 0; j < a.k; ++j) {
-        uint32_t bk = key[0];
-        int bi = 0;
-#pragma unroll
-        for (int i = 1; i < EPL; ++i) {
-            if (key[i] > bk) { bk = key[i]; bi = i; }
-        }
-        const uint32_t gk = group_max<GS>(bk);
-        const uint32_t cand = (bk == gk) ? uint32_t(gl + GS * bi) : 0xffffffffu;
-        const uint32_t ge = group_min<GS>(cand);
-        if (int(ge % GS) == gl) {
-            const int wi = int(ge / GS);
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) if (i == wi) key[i] = 0u;
-        }
-        const float gv = key_value(gk);
-        if (j == 0) vmax = gv;
-        if (gl == j) { my_id = int(ge); my_val = gv; }
-    }
-
-    // Weights in float32. The largest logit is the first pick.
-    const bool mine = gl < a.k;
-    const float ej = mine ? expf(my_val - vmax) : 0.0f;
-    const float denom = a.renorm ? group_sum<GS>(ej)   // sum over the k picks
-                                 : z;                  // sum over all E experts
-    if (valid && mine) {
-        a.topk_ids[(size_t)t * a.k + gl] = my_id;
-        a.topk_weights[(size_t)t * a.k + gl] = ej / denom;
-        return my_id;
-    }
-    return -1;
-}
-
-// Rounds whose (expert, rank) per lane stay in registers until the ranks are
-// finished; later rounds (only for very long token runs) go through inv_perm.
-constexpr int kRegRounds = 4;
-
-// Top-k of the tokens [t0, t1) and the rank of every slot among this warp's
-// slots of the same expert; s_cnt is [NW][E] and counts each warp's picks per
-// expert. Warp w owns tokens [t0 + w*tpw, t0 + (w+1)*tpw); each round takes
-// GPW consecutive tokens, one per lane group, so lane order within a round
-// is slot order. The first kRegRounds rounds return each lane's expert and
-// rank in re/rr (expert -1: no slot); the rank of later rounds is written to
-// inv_perm[s]. The next round's logits are loaded before the current round's
-// selection.
-template <int GS, int EPL, int NT>
-__device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int t1, int32_t* s_cnt,
-                                                int (&re)[kRegRounds], int (&rr)[kRegRounds]) {
-    constexpr int GPW = kWarp / GS;
-    const int lane = threadIdx.x % kWarp;
-    const int warp = threadIdx.x / kWarp;
-    const int grp = lane / GS;
-    const int gl = lane % GS;
-    const unsigned lower = (1u << lane) - 1u;
-    int32_t* cnt = s_cnt + (size_t)warp * a.E;
-    const int w0 = t0 + warp * a.tpw;
-    const int w1 = min(t1, w0 + a.tpw);
-
-    uint32_t key[EPL], next[EPL];
-    load_keys<GS, EPL>(a, w0 + grp, w0 + grp < w1, gl, key);
-#pragma unroll
-    for (int r = 0; r < kRegRounds; ++r) {
-        re[r] = -1;
-        rr[r] = 0;
-        const int tb = w0 + r * GPW;
-        if (tb < w1) {
-            const int tn = tb + GPW + grp;
-            load_keys<GS, EPL>(a, tn, tn < w1, gl, next);
-            const int t = tb + grp;
-            const int e = topk_select<GS, EPL>(a, t, t < w1, gl, key);
-            const unsigned peers = __match_any_sync(kFull, e);
-            re[r] = e;
-            rr[r] = (e >= 0) ? cnt[e] + __popc(peers & lower) : 0;
-            __syncwarp();
-            if (e >= 0 && lane == __ffs(peers) - 1) cnt[e] += __popc(peers);
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) key[i] = next[i];
-        }
-    }
-    for (int tb = w0 + kRegRounds * GPW; tb < w1; tb += GPW) {
-        const int t = tb + grp;
-        const int e = topk_select<GS, EPL>(a, t, t < w1, gl, key);
-        const int tn = tb + GPW + grp;
-        load_keys<GS, EPL>(a, tn, tn < w1, gl, key);
-        const unsigned peers = __match_any_sync(kFull, e);
-        if (e >= 0) a.inv_perm[(size_t)t * a.k + gl] = cnt[e] + __popc(peers & lower);
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) cnt[e] += __popc(peers);
-        __syncwarp();
-    }
-}
-
-// Exclusive scan over warps of s_cnt[w][e] for every expert; s_tot[e] gets
-// the block total.
-template <int NT>
-__device__ __forceinline__ void scan_over_warps(int32_t* s_cnt, int32_t* s_tot, int E) {
-    constexpr int NW = NT / kWarp;
-    for (int e = threadIdx.x; e < E; e += NT) {
-        int run = 0;
-#pragma unroll 4
-        for (int w = 0; w < NW; ++w) {
-            const int v = s_cnt[(size_t)w * E + e];
-            s_cnt[(size_t)w * E + e] = run;
-            run += v;
-        }
-        s_tot[e] = run;
-    }
-}
-
-// Exclusive scan of in[0..n) into out[0..n) (may alias) by a block of NT
-// threads, n <= MOE_MAX_EXPERTS. Uses s_warp[32].
-template <int NT>
-__device__ void block_exclusive_scan(const int32_t* in, int32_t* out, int n, int32_t* s_warp) {
-    constexpr int ITEMS = (1024 + NT - 1) / NT;
-    constexpr int NW = NT / kWarp;
-    const int lane = threadIdx.x % kWarp;
-    const int warp = threadIdx.x / kWarp;
-    const int base = threadIdx.x * ITEMS;
-    int v[ITEMS];
-    int local = 0;
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-        v[i] = (base + i < n) ? in[base + i] : 0;
-        local += v[i];
-    }
-    int x = local;
-#pragma unroll
-    for (int o = 1; o < kWarp; o <<= 1) {
-        const int y = __shfl_up_sync(kFull, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == kWarp - 1) s_warp[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int w = lane < NW ? s_warp[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < kWarp; o <<= 1) {
-            const int y = __shfl_up_sync(kFull, w, o);
-            if (lane >= o) w += y;
-        }
-        s_warp[lane] = w;
-    }
-    __syncthreads();
-    int run = (warp > 0 ? s_warp[warp - 1] : 0) + x - local;
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-        if (base + i < n) out[base + i] = run;
-        run += v[i];
-    }
-    __syncthreads();
-}
-
-// Add each slot's per-warp start to its within-warp rank (s_cnt now holds
-// the exclusive scan over warps). With PLACE (one-block path) the expert's
-// offset is added too, the result is final and perm is written.
-template <int GS, int NT, bool PLACE>
-__device__ __forceinline__ void finish_ranks(const RouteArgs& a, int t0, int t1, const int32_t* s_cnt,
-                                             const int32_t* s_off, const int (&re)[kRegRounds],
-                                             const int (&rr)[kRegRounds]) {
-    constexpr int GPW = kWarp / GS;
-    const int lane = threadIdx.x % kWarp;
-    const int warp = threadIdx.x / kWarp;
-    const int grp = lane / GS;
-    const int gl = lane % GS;
-    const int32_t* start = s_cnt + (size_t)warp * a.E;
-    const int w0 = t0 + warp * a.tpw;
-    const int w1 = min(t1, w0 + a.tpw);
-#pragma unroll
-    for (int r = 0; r < kRegRounds; ++r) {
-        if (re[r] >= 0) {
-            const int s = (w0 + r * GPW + grp) * a.k + gl;
-            int p = rr[r] + start[re[r]];
-            if constexpr (PLACE) {
-                p += s_off[re[r]];
-                a.perm[p] = s;
-            }
-            a.inv_perm[s] = p;
-        }
-    }
-    // slots of rounds past kRegRounds: the rank was kept in inv_perm
-    const int s_lo = (w0 + kRegRounds * GPW) * a.k;
-    for (int s = s_lo + lane; s < w1 * a.k; s += kWarp) {
-        const int e = __ldcg(a.topk_ids + s);
-        int p = __ldcg(a.inv_perm + s) + start[e];
-        if constexpr (PLACE) {
-            p += s_off[e];
-            a.perm[p] = s;
-        }
-        a.inv_perm[s] = p;
-    }
-}
 
 template <int GS, int EPL, int NT>
 __global__ void __launch_bounds__(NT) route_rank_kernel(RouteArgs a) {
@@ -536,6 +242,7 @@ cudaError_t launch_route(const RoutePlan& plan, const float* logits, int T, int 
     a.expert_counts = expert_counts; a.expert_offsets = expert_offsets;
     a.perm = perm; a.inv_perm = inv_perm;
     a.ws_counts = static_cast<int32_t*>(workspace);
+    a.write_out = true;
     switch (plan.gs * 100 + plan.epl) {
         case 801: return launch_route_t<8, 1>(plan, a, stream);
         case 1601: return launch_route_t<16, 1>(plan, a, stream);

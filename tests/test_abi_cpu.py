@@ -136,6 +136,25 @@ def test_expand_swiglu_combine_reject_bad_arguments(lib):
     assert lib.moe_combine(0, 0, 256, 2, 0, 0, 0, None) == OK
 
 
+def test_route_expand_rejects_bad_arguments(lib):
+    def call(T=16, E=64, k=4, H=256, x=A[7], ex=A[8], ws=0, ws_bytes=0, p=None):
+        p = list(A[:7]) if p is None else p
+        return lib.moe_route_expand(p[0], T, E, k, 1, x, H, p[1], p[2], p[3], p[4], p[5], p[6],
+                                    ex, ws, ws_bytes, None)
+    assert call(H=250) == MISALIGNED                       # H % 8
+    assert call(x=A[7] + 8) == MISALIGNED                  # bf16 rows need 16-byte alignment
+    assert call(ex=0) == INVALID
+    assert call(x=0) == INVALID
+    assert call(k=0) == INVALID
+    assert call(E=2000) == UNSUPPORTED
+    assert call(ex=A[0]) == INVALID                        # expanded_x over the logits
+    assert call(x=A[1]) == INVALID                         # an output over x
+    assert call(T=4096, E=128, k=8) == WORKSPACE           # two-kernel path without workspace
+    p = list(A[:7])
+    p[3] = 0
+    assert call(p=p) == INVALID
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     from memory_bound_moe_gb300 import moe_swiglu

@@ -345,3 +345,41 @@ def test_parity_check_catches_a_single_flipped_element(dev, O):
     bad["perm"][[0, 1]] = bad["perm"][[1, 0]]
     with pytest.raises(AssertionError):
         assert_route_equal(g, bad, "planted swap")
+
+
+# ---------------------------------------------------------------------------
+# route + expand in one call (one launch for decode-sized batches)
+# ---------------------------------------------------------------------------
+
+ROUTE_EXPAND_CASES = [
+    # T, E, k, H, renorm  (the first rows take the one-launch path)
+    (1, 8, 2, 64, True), (7, 3, 3, 24, True), (16, 256, 8, 7168, False), (32, 64, 4, 2880, True),
+    (64, 8, 2, 256, True), (128, 8, 8, 16, False), (5, 1024, 16, 512, True), (30, 16, 5, 8, True),
+    (33, 64, 4, 256, True), (1023, 32, 4, 2880, True),       # two-kernel route + expand
+]
+
+
+@pytest.mark.parametrize("T,E,k,H,renorm", ROUTE_EXPAND_CASES)
+@pytest.mark.parametrize("wide", [True, False])
+def test_route_expand_matches_oracle_and_separate_calls(dev, O, T, E, k, H, renorm, wide):
+    from memory_bound_moe_gb300 import moe_expand, moe_route, moe_route_expand
+    logits = _logits(T, E, "ties" if T % 2 else "normal", seed=T + E + H)
+    x = _rand_bf16(O, (T, H), seed=H + k)
+    ld = torch.from_numpy(logits).to(dev)
+    xd = bf16_dev(x, dev)
+    expanded = torch.full((T * k, H), -1, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    if not wide:
+        xd = _offset16(xd)
+        expanded = _offset16(expanded)
+    r, ex = moe_route_expand(ld, xd, k, renorm, expanded=expanded)
+    torch.cuda.synchronize()
+    ref = O.route(logits, k, renorm)
+    assert_route_equal({f: getattr(r, f).cpu().numpy() for f in r._fields}, ref, f"T={T} E={E}")
+    check_exact(u16(ex), O.expand(x, k, ref["perm"]), f"expanded T={T} E={E} k={k} H={H}")
+    # bit-identical to the two separate calls
+    r2 = moe_route(ld, k, renorm)
+    ex2 = moe_expand(xd, r2.inv_perm, k)
+    torch.cuda.synchronize()
+    for f in r._fields:
+        assert torch.equal(getattr(r, f), getattr(r2, f)), f
+    assert torch.equal(ex.view(torch.int16), ex2.view(torch.int16))
