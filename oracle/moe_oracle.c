@@ -179,17 +179,73 @@ int oracle_route_permute(const int32_t* topk_ids, long T, int E, int k,
 }
 
 /* ---------------------------------------------------------------------- */
+/* Local permutation: one expert range, padded expert segments             */
+/* ---------------------------------------------------------------------- */
+
+/* "CuTeDSL at Perplexity", section "Mixture of Experts (MoE) dispatch/combine",
+ * sub-section "Single node": with tensor parallelism the inputs are
+ * replicated and a rank's dispatch routes only the tokens assigned to the
+ * experts it holds; its combine sums the local copies and an all-reduce adds
+ * the ranks' partial results. Sub-section "Local": the tokens are copied
+ * into an optionally padded buffer for the expert GEMM.
+ * Reading: the top-k is over all E experts (topk_ids are global); this rank
+ * holds experts [e0, e1), n = e1 - e0; every local expert's segment is
+ * rounded up to a multiple of pad (pad = 1: no padding).
+ *   local slots      s with e_s in [e0, e1), local expert l_s = e_s - e0
+ *   counts[l]        = #{ local s : l_s = l }                         [n]
+ *   offsets[0] = 0,  offsets[l+1] = offsets[l] + pad * ceil(counts[l] / pad)
+ *   inv_perm[s]      = offsets[l_s] + #{ local s' < s : l_s' = l_s }, and -1
+ *                      for slots whose expert is not local           [T*k]
+ *   perm[p]          = s for those rows, -1 for every other row p < rows
+ * rows must be at least offsets[n]. Returns -1 on bad arguments. */
+int oracle_route_permute_local(const int32_t* topk_ids, long T, int E, int k, int e0, int e1,
+                               int pad, long rows, int32_t* counts, int32_t* offsets,
+                               int32_t* perm, int32_t* inv_perm) {
+    if (e0 < 0 || e1 > E || e0 >= e1 || pad < 1) return -1;
+    const int n = e1 - e0;
+    const long S = T * (long)k;
+    for (int l = 0; l < n; ++l) counts[l] = 0;
+    for (long s = 0; s < S; ++s) {
+        int32_t e = topk_ids[s];
+        if (e < 0 || e >= E) return -1;
+        if (e >= e0 && e < e1) counts[e - e0] += 1;
+    }
+    offsets[0] = 0;
+    for (int l = 0; l < n; ++l)
+        offsets[l + 1] = offsets[l] + (int32_t)(((long)counts[l] + pad - 1) / pad * pad);
+    if ((long)offsets[n] > rows) return -1;
+    for (long p = 0; p < rows; ++p) perm[p] = -1;
+    int32_t* next = (int32_t*)malloc(sizeof(int32_t) * (size_t)n);
+    if (!next) return -1;
+    for (int l = 0; l < n; ++l) next[l] = offsets[l];
+    for (long s = 0; s < S; ++s) {
+        int32_t e = topk_ids[s];
+        if (e >= e0 && e < e1) {
+            int32_t pos = next[e - e0]++;
+            perm[pos] = (int32_t)s;
+            inv_perm[s] = pos;
+        } else {
+            inv_perm[s] = -1;
+        }
+    }
+    free(next);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
 /* Expand: expert-sorted copy of token rows                                */
 /* ---------------------------------------------------------------------- */
 
 /* expanded_x[p, :] = x[perm[p] / k, :] for p in [0, P). Bit copy.
+ * Rows with perm[p] < 0 (padding, or no local slot) are left as they are.
  * P may be smaller than T*k to produce a contiguous block of rows
  * (pass perm + p0). Returns -1 if a source token falls outside [0, T). */
 int oracle_expand(const uint16_t* x, long T, int H, int k,
                   const int32_t* perm, long P, uint16_t* expanded_x) {
     for (long p = 0; p < P; ++p) {
+        if (perm[p] < 0) continue;
         long t = (long)perm[p] / k;
-        if (perm[p] < 0 || t >= T) return -1;
+        if (t >= T) return -1;
         memcpy(expanded_x + p * (long)H, x + t * (long)H, sizeof(uint16_t) * (size_t)H);
     }
     return 0;
@@ -219,10 +275,12 @@ void oracle_swiglu(const uint16_t* gate_up, long rows, int I, uint16_t* act) {
 /* ---------------------------------------------------------------------- */
 
 /* out[t, :] = bf16( sum_{j<k} w[t, j] * expert_out[inv_perm[t*k + j], :] ),
- * summed in real arithmetic for j = 0..k-1 and rounded once.
+ * summed in real arithmetic for j = 0..k-1 and rounded once. A negative
+ * inv_perm entry (a slot whose expert another rank holds) contributes
+ * nothing: the result is then this rank's partial sum.
  * S is the number of rows of expert_out (for the range check); T may be a
  * sub-range of tokens if w and inv_perm are offset to match.
- * Returns -1 if a row index falls outside [0, S). */
+ * Returns -1 if a row index is S or more. */
 int oracle_combine(const uint16_t* expert_out, long S, int H, int k, long T,
                    const float* w, const int32_t* inv_perm, uint16_t* out) {
     double* acc = (double*)malloc(sizeof(double) * (size_t)H);
@@ -231,7 +289,8 @@ int oracle_combine(const uint16_t* expert_out, long S, int H, int k, long T,
         for (int c = 0; c < H; ++c) acc[c] = 0.0;
         for (int j = 0; j < k; ++j) {
             long p = inv_perm[t * k + j];
-            if (p < 0 || p >= S) { free(acc); return -1; }
+            if (p < 0) continue;
+            if (p >= S) { free(acc); return -1; }
             double wj = (double)w[t * k + j];
             const uint16_t* row = expert_out + p * (long)H;
             for (int c = 0; c < H; ++c) acc[c] += wj * bf16_to_double(row[c]);

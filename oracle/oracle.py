@@ -62,6 +62,10 @@ def _load():
         lib.oracle_route_permute.argtypes = [_i32p, ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                              _i32p, _i32p, _i32p, _i32p]
         lib.oracle_route_permute.restype = ctypes.c_int
+        lib.oracle_route_permute_local.argtypes = [_i32p, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_long, _i32p, _i32p, _i32p, _i32p]
+        lib.oracle_route_permute_local.restype = ctypes.c_int
         lib.oracle_expand.argtypes = [_u16p, ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                       _i32p, ctypes.c_long, _u16p]
         lib.oracle_expand.restype = ctypes.c_int
@@ -147,6 +151,48 @@ def route(logits, k: int, renorm: bool):
     counts, offsets, perm, inv_perm = route_permute(ids, E)
     return {"topk_ids": ids, "topk_weights": w, "expert_counts": counts,
             "expert_offsets": offsets, "perm": perm, "inv_perm": inv_perm}
+
+
+def local_rows_capacity(T: int, k: int, n_local: int, pad: int) -> int:
+    """Rows a padded local buffer may need at most: every slot local, every
+    local expert's segment padded by pad - 1."""
+    return T * k + n_local * (pad - 1)
+
+
+def route_permute_local(topk_ids, E: int, e0: int, e1: int, pad: int, rows: int = None):
+    """Permutation of the slots whose expert lies in [e0, e1), each local
+    expert's segment padded to a multiple of pad. Returns (counts [n],
+    offsets [n+1], perm [rows], inv_perm [S]); -1 marks padding rows in perm
+    and non-local slots in inv_perm."""
+    ids = _c(topk_ids, np.int32)
+    T, k = ids.shape
+    n = e1 - e0
+    if rows is None:
+        rows = local_rows_capacity(T, k, n, pad)
+    counts = np.empty(n, dtype=np.int32)
+    offsets = np.empty(n + 1, dtype=np.int32)
+    perm = np.empty(rows, dtype=np.int32)
+    inv_perm = np.empty(T * k, dtype=np.int32)
+    rc = _load().oracle_route_permute_local(_ptr(ids, ctypes.c_int32), T, E, k, e0, e1, pad, rows,
+                                            _ptr(counts, ctypes.c_int32), _ptr(offsets, ctypes.c_int32),
+                                            _ptr(perm, ctypes.c_int32), _ptr(inv_perm, ctypes.c_int32))
+    if rc != 0:
+        raise ValueError("oracle_route_permute_local: bad arguments")
+    return counts, offsets, perm, inv_perm
+
+
+def expand_into(x, k: int, perm, out) -> np.ndarray:
+    """Like expand(), writing into ``out`` and leaving rows with perm < 0 as
+    they are."""
+    x = _c(x, np.uint16)
+    perm = _c(perm, np.int32)
+    T, H = x.shape
+    assert out.flags["C_CONTIGUOUS"] and out.dtype == np.uint16 and out.shape == (perm.size, H)
+    rc = _load().oracle_expand(_ptr(x, ctypes.c_uint16), T, H, k, _ptr(perm, ctypes.c_int32), perm.size,
+                               _ptr(out, ctypes.c_uint16))
+    if rc != 0:
+        raise ValueError("oracle_expand: source token out of range")
+    return out
 
 
 def expand(x, k: int, perm) -> np.ndarray:

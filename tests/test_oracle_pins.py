@@ -390,3 +390,86 @@ def test_combine_matches_numpy_weighted_sum(oracle_mod):
     t0, t1 = 10, 20
     part = oracle_mod.combine(eo, w[t0:t1], r["inv_perm"][t0 * k:t1 * k])
     assert np.array_equal(part, ours[t0:t1])
+
+
+# ---------------------------------------------------------------------------
+# local (expert-range) routing with padded segments
+# ---------------------------------------------------------------------------
+
+def test_route_local_hand_worked_example(oracle_mod):
+    base = read_fixture("route_hand_worked.txt")
+    fx = read_fixture("route_local_hand_worked.txt")
+    T, E, k = int(base["T"][0]), int(base["E"][0]), int(base["k"][0])
+    ids = np.array([int(v) for v in base["topk_ids"]], dtype=np.int32).reshape(T, k)
+    e0, e1, pad, rows = (int(fx[n][0]) for n in ("e0", "e1", "pad", "rows"))
+    counts, offsets, perm, inv = oracle_mod.route_permute_local(ids, E, e0, e1, pad, rows)
+    assert counts.tolist() == [int(v) for v in fx["counts"]]
+    assert offsets.tolist() == [int(v) for v in fx["offsets"]]
+    assert perm.tolist() == [int(v) for v in fx["perm"]]
+    assert inv.tolist() == [int(v) for v in fx["inv_perm"]]
+    assert oracle_mod.local_rows_capacity(T, k, e1 - e0, pad) == rows
+
+
+@pytest.mark.parametrize("T,E,k", [(37, 8, 2), (200, 64, 8), (129, 32, 4)])
+def test_route_local_full_range_without_padding_is_the_full_routing(oracle_mod, T, E, k):
+    rng = np.random.default_rng(T)
+    r = oracle_mod.route(rng.standard_normal((T, E)).astype(np.float32), k, True)
+    counts, offsets, perm, inv = oracle_mod.route_permute_local(r["topk_ids"], E, 0, E, 1)
+    assert np.array_equal(counts, r["expert_counts"])
+    assert np.array_equal(offsets, r["expert_offsets"])
+    assert np.array_equal(perm, r["perm"])
+    assert np.array_equal(inv, r["inv_perm"])
+
+
+@pytest.mark.parametrize("pad", [1, 4, 128])
+def test_route_local_partition_matches_global_segments(oracle_mod, pad):
+    # split the experts into ranges (ranks); every rank's rows in order are the
+    # global permutation's segment for its experts, padding aside
+    T, E, k = 300, 32, 4
+    rng = np.random.default_rng(pad)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[:, :3] += 2.0
+    r = oracle_mod.route(logits, k, True)
+    g_off = r["expert_offsets"]
+    seen = np.zeros(T * k, dtype=int)
+    for e0, e1 in [(0, 5), (5, 6), (6, 20), (20, 32)]:
+        counts, offsets, perm, inv = oracle_mod.route_permute_local(r["topk_ids"], E, e0, e1, pad)
+        assert np.array_equal(counts, r["expert_counts"][e0:e1])
+        assert np.all(offsets % pad == 0)
+        slack = np.diff(offsets) - counts
+        assert np.all((slack >= 0) & (slack < pad))
+        rows_used = perm[perm >= 0]
+        assert np.array_equal(rows_used, r["perm"][g_off[e0]:g_off[e1]])
+        local = (r["topk_ids"].ravel() >= e0) & (r["topk_ids"].ravel() < e1)
+        assert np.all(inv[~local] == -1)
+        assert np.array_equal(perm[inv[local]], np.flatnonzero(local))
+        for l in range(e1 - e0):                          # padding rows are -1
+            assert np.all(perm[offsets[l] + counts[l]:offsets[l + 1]] == -1)
+        assert np.all(perm[offsets[-1]:] == -1)
+        seen[local] += 1
+    assert np.all(seen == 1)                              # every slot on exactly one rank
+
+
+def test_combine_partial_sums_skip_other_ranks(oracle_mod):
+    # a rank's partial combine (-1 for slots it does not hold) equals the full
+    # combine with the other ranks' weights set to zero, and the partials of
+    # all ranks add up (in real arithmetic) to the full combine
+    T, H, E, k = 40, 64, 16, 4
+    rng = np.random.default_rng(3)
+    r = oracle_mod.route(rng.standard_normal((T, E)).astype(np.float32), k, True)
+    eo_full = oracle_mod.bf16_round(rng.standard_normal((T * k, H)))
+    ids = r["topk_ids"]
+    total = np.zeros((T, H))
+    mag = np.zeros((T, H))
+    for e0, e1 in [(0, 7), (7, 16)]:
+        counts, offsets, perm, inv = oracle_mod.route_permute_local(ids, E, e0, e1, 8)
+        eo = np.zeros((perm.size, H), dtype=np.uint16)
+        eo[perm >= 0] = eo_full[r["inv_perm"][perm[perm >= 0]]]   # each local row's data
+        part = oracle_mod.combine(eo, r["topk_weights"], inv)
+        w0 = r["topk_weights"] * ((ids >= e0) & (ids < e1))
+        assert np.array_equal(part, oracle_mod.combine(eo_full, w0, r["inv_perm"]))
+        total += bf16_bits_to_f64(part)
+        mag += np.abs(bf16_bits_to_f64(part))
+    full = bf16_bits_to_f64(oracle_mod.combine(eo_full, r["topk_weights"], r["inv_perm"]))
+    # each partial and the full result are rounded once (half a bf16 ulp each)
+    assert np.all(np.abs(total - full) <= 2 ** -8 * (mag + np.abs(full)))
