@@ -271,6 +271,87 @@ void oracle_swiglu(const uint16_t* gate_up, long rows, int I, uint16_t* act) {
 }
 
 /* ---------------------------------------------------------------------- */
+/* MXFP8 block quantization (E4M3 elements, one E8M0 scale per 32)         */
+/* ---------------------------------------------------------------------- */
+
+/* "CuTeDSL at Perplexity", section "Blackwell support": Blackwell adds
+ * hardware support for MXFP8, MXFP4 and NVFP4; the kernels were adapted for
+ * FP8 block-wise scaling, computing the absolute maximum over blocks of 32
+ * elements (MXFP8/MXFP4) or 16 (NVFP4). The pages give no formula; the
+ * definition followed is the OCP Microscaling (MX) Formats Specification
+ * v1.0 (MXFP8 E4M3): for a block of 32 values with absolute maximum amax,
+ *   X       = floor(log2(amax)) - 8        (8: largest normal exponent of E4M3)
+ *             clamped to [-127, 127]; amax = 0 gives X = -127
+ *   scale   = 2^X, stored as the E8M0 byte X + 127
+ *   code_i  = E4M3(v_i / 2^X), round to nearest even, saturating to +-448
+ * The values quantized here are bfloat16 (the rows the GEMM would read), so
+ * every step is exact up to the final E4M3 rounding. */
+
+/* E4M3 (1 sign, 4 exponent bits with bias 7, 3 fraction bits; no infinity,
+ * 0x7F/0xFF NaN, largest finite 448): round a real to the nearest E4M3 value,
+ * ties to even, magnitudes beyond 448 saturate to 448. The spacing around
+ * |v| in [2^e, 2^(e+1)) is 2^(max(e,-6)-3). */
+static uint8_t e4m3_round(double v) {
+    if (isnan(v)) return (uint8_t)0x7F;
+    uint8_t sign = signbit(v) ? (uint8_t)0x80 : (uint8_t)0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    int e2;
+    (void)frexp(a, &e2);
+    int lead = e2 - 1;
+    if (lead < -6) lead = -6;
+    double spacing = ldexp(1.0, lead - 3);
+    double r = rint(a / spacing) * spacing;
+    if (r >= 448.0) return (uint8_t)(sign | 0x7E);
+    if (r == 0.0) return sign;
+    /* encode r: normal if r >= 2^-6 */
+    int re2;
+    double f = frexp(r, &re2);          /* r = f * 2^re2, f in [0.5, 1) */
+    int ex = re2 - 1;                    /* r = 1.m * 2^ex */
+    if (ex < -6) {                       /* subnormal: r = m/8 * 2^-6 */
+        int m = (int)(r / ldexp(1.0, -9));
+        return (uint8_t)(sign | (uint8_t)m);
+    }
+    int m = (int)((f * 2.0 - 1.0) * 8.0);
+    return (uint8_t)(sign | (uint8_t)((ex + 7) << 3) | (uint8_t)m);
+}
+
+void oracle_e4m3_round(const double* in, long n, uint8_t* out) {
+    for (long i = 0; i < n; ++i) out[i] = e4m3_round(in[i]);
+}
+
+/* Shared exponent X of a block (see above). */
+static int mx_exponent(double amax) {
+    if (amax == 0.0) return -127;
+    int e2;
+    (void)frexp(amax, &e2);              /* floor(log2(amax)) = e2 - 1 */
+    int x = (e2 - 1) - 8;
+    if (x < -127) x = -127;
+    if (x > 127) x = 127;
+    return x;
+}
+
+/* MXFP8 quantization of a [rows, n] bfloat16 matrix (n a multiple of 32):
+ * codes [rows, n] E4M3 bytes, scales [rows, n/32] E8M0 bytes. */
+void oracle_quant_mxfp8(const uint16_t* in, long rows, int n, uint8_t* codes, uint8_t* scales) {
+    for (long r = 0; r < rows; ++r) {
+        for (int b = 0; b < n / 32; ++b) {
+            const uint16_t* v = in + r * (long)n + b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                double a = fabs(bf16_to_double(v[i]));
+                if (a > amax) amax = a;
+            }
+            int x = mx_exponent(amax);
+            scales[r * (long)(n / 32) + b] = (uint8_t)(x + 127);
+            for (int i = 0; i < 32; ++i)
+                codes[r * (long)n + b * 32 + i] = e4m3_round(ldexp(bf16_to_double(v[i]), -x));
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------- */
 /* Combine: weighted sum of each token's k expert rows                     */
 /* ---------------------------------------------------------------------- */
 

@@ -66,6 +66,11 @@ def _load():
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    ctypes.c_long, _i32p, _i32p, _i32p, _i32p]
         lib.oracle_route_permute_local.restype = ctypes.c_int
+        lib.oracle_e4m3_round.argtypes = [_f64p, ctypes.c_long, ctypes.POINTER(ctypes.c_uint8)]
+        lib.oracle_e4m3_round.restype = None
+        lib.oracle_quant_mxfp8.argtypes = [_u16p, ctypes.c_long, ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_uint8)]
+        lib.oracle_quant_mxfp8.restype = None
         lib.oracle_expand.argtypes = [_u16p, ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                       _i32p, ctypes.c_long, _u16p]
         lib.oracle_expand.restype = ctypes.c_int
@@ -234,6 +239,47 @@ def combine(expert_out, topk_weights, inv_perm) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle_combine: row index out of range")
     return out
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Round reals to E4M3 bytes (nearest even, saturating to +-448)."""
+    v = _c(v, np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e4m3_round(_ptr(v, ctypes.c_double), v.size, _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def e4m3_decode(b) -> np.ndarray:
+    """E4M3 bytes -> float64 (0x7F/0xFF are NaN). A table written from the
+    format's definition (sign, 4-bit exponent with bias 7, 3-bit fraction)."""
+    b = np.asarray(b, dtype=np.uint8)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e.astype(np.float64) - 7))
+    val = np.where((b & 0x7F) == 0x7F, np.nan, val)
+    return sign * val
+
+
+def quant_mxfp8(x_bf16):
+    """MXFP8 quantization of a [rows, n] bfloat16 matrix (n % 32 == 0):
+    returns (codes uint8 [rows, n], scales uint8 [rows, n/32])."""
+    x = _c(x_bf16, np.uint16)
+    rows, n = x.shape
+    assert n % 32 == 0
+    codes = np.empty((rows, n), dtype=np.uint8)
+    scales = np.empty((rows, n // 32), dtype=np.uint8)
+    _load().oracle_quant_mxfp8(_ptr(x, ctypes.c_uint16), rows, n, _ptr(codes, ctypes.c_uint8),
+                               _ptr(scales, ctypes.c_uint8))
+    return codes, scales
+
+
+def dequant_mxfp8(codes, scales) -> np.ndarray:
+    """codes * 2^(scale - 127), float64."""
+    codes = np.asarray(codes)
+    rows, n = codes.shape
+    x = np.asarray(scales).astype(np.float64) - 127.0
+    return e4m3_decode(codes) * np.repeat(2.0 ** x, 32, axis=1).reshape(rows, n)
 
 
 def path(logits, x, gate_up, expert_out, k: int, renorm: bool):

@@ -473,3 +473,75 @@ def test_combine_partial_sums_skip_other_ranks(oracle_mod):
     full = bf16_bits_to_f64(oracle_mod.combine(eo_full, r["topk_weights"], r["inv_perm"]))
     # each partial and the full result are rounded once (half a bf16 ulp each)
     assert np.all(np.abs(total - full) <= 2 ** -8 * (mag + np.abs(full)))
+
+
+# ---------------------------------------------------------------------------
+# MXFP8 (E4M3 elements, E8M0 scale per 32)
+# ---------------------------------------------------------------------------
+
+def test_e4m3_round_known_patterns(oracle_mod):
+    cases = [(448.0, 0x7E), (1.0, 0x38), (0.5, 0x30), (2.0 ** -6, 0x08), (2.0 ** -9, 0x01),
+             (2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02), (464.0, 0x7E), (1e9, 0x7E), (-448.0, 0xFE),
+             (1.0625, 0x38), (1.1875, 0x3A), (0.0, 0x00), (-0.0, 0x80), (240.0, 0x77),
+             (7 * 2.0 ** -9, 0x07), (-3.0, 0xC4), (math.inf, 0x7E)]   # -3 = -1.5*2^1: 0x80|8<<3|4
+    got = oracle_mod.e4m3_round(np.array([v for v, _ in cases]))
+    assert [int(g) for g in got] == [b for _, b in cases]
+
+
+def test_e4m3_matches_torch_in_range(oracle_mod):
+    fp8 = getattr(torch, "float8_e4m3fn", None)
+    if fp8 is None:
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(0)
+    v = np.concatenate([rng.standard_normal(100_000) * 50, rng.standard_normal(20_000) * 1e-2,
+                        rng.uniform(-448, 448, 20_000)]).astype(np.float32)
+    ours = oracle_mod.e4m3_round(v.astype(np.float64))
+    ref = torch.from_numpy(v).to(fp8).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(ours, ref)
+    codes = np.arange(256, dtype=np.uint8)
+    dec = oracle_mod.e4m3_decode(codes)
+    tref = torch.from_numpy(codes).view(fp8).to(torch.float64).numpy()
+    nan = np.isnan(tref)
+    assert np.array_equal(np.isnan(dec), nan)
+    np.testing.assert_array_equal(dec[~nan], tref[~nan])
+
+
+def test_mxfp8_scales_closed_forms(oracle_mod):
+    O = oracle_mod
+    rows = np.zeros((5, 64))
+    rows[0, :32] = 448.0                   # amax 448: X = 0, byte 127, codes 0x7E
+    rows[0, 32:] = 0.0                     # zero block: byte 0, codes 0
+    rows[1, :32] = 1.0                     # amax 1: X = -8, 1 / 2^-8 = 256 = 0x78
+    rows[1, 32:] = np.linspace(-0.75, 0.75, 32)   # amax 0.75: X = -9
+    rows[2, :32] = 2.0 ** -130             # tiny (bf16 subnormal): X clamps to -127
+    rows[2, 32:] = 500.0                   # amax 500: X = 0; 500 saturates to 448
+    rows[3, :] = np.arange(64) - 31.5      # amax 31.5 / 32: X = -4
+    rows[4, :] = 3.0e38                    # near the top of the bf16 range: X = 119
+    x = O.bf16_round(rows)
+    codes, scales = O.quant_mxfp8(x)
+    assert scales.tolist() == [[127, 0], [119, 118], [0, 127], [123, 123], [246, 246]]
+    assert np.all(codes[0, :32] == 0x7E) and np.all(codes[0, 32:] == 0)
+    assert np.all(codes[1, :32] == 0x78)
+    assert np.all(codes[2, 32:] == 0x7E)
+    assert np.all(codes[2, :32] == O.e4m3_round(np.full(32, 2.0 ** -130 * 2.0 ** 127)))
+
+
+def test_mxfp8_round_trip_error_bound(oracle_mod):
+    O = oracle_mod
+    rng = np.random.default_rng(1)
+    v = rng.standard_normal((64, 256)) * np.exp(rng.uniform(-12, 12, (64, 1)))
+    x = O.bf16_round(v)
+    xv = O.bf16_decode(x)
+    codes, scales = O.quant_mxfp8(x)
+    deq = O.dequant_mxfp8(codes, scales)
+    X = np.repeat(scales.astype(np.float64) - 127, 32, axis=1)
+    scaled = np.abs(xv) / 2.0 ** X
+    # every block's largest magnitude lands in [256, 512)
+    amax_scaled = scaled.reshape(64, 8, 32).max(axis=2)
+    assert np.all((amax_scaled >= 256) & (amax_scaled < 512))
+    inside = scaled <= 448
+    # half an E4M3 ulp: 2^-4 relative for normals, 2^-10 * 2^X for subnormals
+    bound = np.maximum(2.0 ** -4 * np.abs(xv), 2.0 ** (X - 10))
+    assert np.all(np.abs(deq - xv)[inside] <= bound[inside])
+    assert np.all(np.abs(deq[~inside]) == 448 * 2.0 ** X[~inside])
+    assert np.all(np.sign(deq) * np.sign(xv) >= 0)
