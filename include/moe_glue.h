@@ -185,6 +185,45 @@ moe_status_t moe_route_static(const float* logits, int64_t T, int E, int k, int 
                               moe_stream_t stream);
 
 /*
+ * Local routing for one tensor-parallel rank: experts [e0, e1) only, with
+ * every local expert's segment padded to a multiple of pad.
+ * "CuTeDSL at Perplexity", section "Mixture of Experts (MoE) dispatch/combine",
+ * sub-section "Single node": with tensor parallelism the routing information
+ * and the tokens are replicated; a rank's dispatch routes only the tokens
+ * assigned to the experts it holds (the local kernel reused with a small
+ * change), its combine sums the local copies and an all-reduce across ranks
+ * adds the partial results. Sub-section "Local": the tokens go to an
+ * optionally padded buffer for the MoE GEMM.
+ *
+ * The top-k runs over all E experts, so topk_ids/topk_weights are exactly
+ * those of moe_route. With n = e1 - e0 and local slots s (e_s in [e0, e1)):
+ *   expert_counts[l]  = #{ local s : e_s = e0 + l }                    [n]
+ *   expert_offsets[0] = 0, expert_offsets[l+1] = expert_offsets[l] +
+ *                       pad * ceil(expert_counts[l] / pad)               [n + 1]
+ *   inv_perm[s]       = expert_offsets[e_s - e0] + #{ local s' < s with
+ *                       the same expert }, or -1 if e_s is not local    [T*k]
+ *   perm[p]           = s for those rows and -1 for every other row     [rows]
+ * where rows = moe_route_local_rows(T, k, e0, e1, pad) = T*k + n*(pad-1),
+ * the most rows a padded local buffer can need. With e0 = 0, e1 = E, pad = 1
+ * every output equals moe_route's. workspace: at least
+ * moe_route_local_workspace_size(T, E, k, e0, e1) bytes (0: may be NULL).
+ * Use moe_expand_rows / moe_combine_rows with `rows` rows; the combine then
+ * yields this rank's partial sum (slots with inv_perm -1 contribute nothing).
+ * Errors: as moe_route, plus MOE_ERR_INVALID_ARG unless 0 <= e0 < e1 <= E
+ * and pad >= 1, MOE_ERR_UNSUPPORTED if rows >= 2^31.
+ */
+moe_status_t moe_route_local_rows(int64_t T, int k, int e0, int e1, int pad, int64_t* rows);
+moe_status_t moe_route_local_workspace_size(int64_t T, int E, int k, int e0, int e1,
+                                            size_t* bytes);
+moe_status_t moe_route_local(const float* logits, int64_t T, int E, int k, int renorm,
+                             int e0, int e1, int pad,
+                             int32_t* topk_ids, float* topk_weights,
+                             int32_t* expert_counts, int32_t* expert_offsets,
+                             int32_t* perm, int32_t* inv_perm,
+                             void* workspace, size_t workspace_bytes,
+                             moe_stream_t stream);
+
+/*
  * Row expansion into expert order (expandInputRows).
  * "CuTeDSL at Perplexity", section "Mixture of Experts (MoE) dispatch/combine",
  * sub-section "Local" (tokens are copied to the buffer the MoE GEMM reads),
@@ -201,6 +240,15 @@ moe_status_t moe_route_static(const float* logits, int64_t T, int E, int k, int 
 moe_status_t moe_expand(const moe_bf16_t* x, int64_t T, int H, int k,
                         const int32_t* inv_perm, moe_bf16_t* expanded_x,
                         moe_stream_t stream);
+
+/*
+ * moe_expand into a buffer of `rows` rows (a padded local buffer): entries of
+ * inv_perm outside [0, rows), such as the -1 of slots another rank holds, are
+ * skipped, and rows no slot maps to (padding) are left as they are.
+ */
+moe_status_t moe_expand_rows(const moe_bf16_t* x, int64_t T, int H, int k,
+                             const int32_t* inv_perm, int64_t rows, moe_bf16_t* expanded_x,
+                             moe_stream_t stream);
 
 /*
  * Gated SwiGLU activation (doActivation).
@@ -234,6 +282,16 @@ moe_status_t moe_swiglu(const moe_bf16_t* gate_up, int64_t rows, int I,
 moe_status_t moe_combine(const moe_bf16_t* expert_out, int64_t T, int H, int k,
                          const float* topk_weights, const int32_t* inv_perm,
                          moe_bf16_t* out, moe_stream_t stream);
+
+/*
+ * moe_combine over an expert_out of `rows` rows (a padded local buffer):
+ * entries of inv_perm outside [0, rows), such as -1, contribute nothing, so
+ * after moe_route_local the result is this rank's partial sum, to be added
+ * across ranks (the all-reduce is not part of this library).
+ */
+moe_status_t moe_combine_rows(const moe_bf16_t* expert_out, int64_t rows, int64_t T, int H, int k,
+                              const float* topk_weights, const int32_t* inv_perm,
+                              moe_bf16_t* out, moe_stream_t stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

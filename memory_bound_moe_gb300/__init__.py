@@ -10,9 +10,11 @@ Python or CPU fallback, and a missing library is an error.
 from __future__ import annotations
 
 from .binding import (MoeError, RouteResult, STATUS, library_path, load_library, moe_combine,
-                      moe_expand, moe_route, moe_route_expand, moe_route_workspace_size, moe_status_string,
-                      moe_swiglu)
+                      moe_combine_rows, moe_expand, moe_expand_rows, moe_route, moe_route_expand,
+                      moe_route_local, moe_route_local_rows, moe_route_local_workspace_size,
+                      moe_route_workspace_size, moe_status_string, moe_swiglu)
 
 __all__ = ["MoeError", "RouteResult", "STATUS", "library_path", "load_library", "moe_combine",
-           "moe_expand", "moe_route", "moe_route_expand", "moe_route_workspace_size", "moe_status_string",
-           "moe_swiglu"]
+           "moe_combine_rows", "moe_expand", "moe_expand_rows", "moe_route", "moe_route_expand",
+           "moe_route_local", "moe_route_local_rows", "moe_route_local_workspace_size",
+           "moe_route_workspace_size", "moe_status_string", "moe_swiglu"]

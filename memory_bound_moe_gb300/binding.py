@@ -60,6 +60,18 @@ def load_library():
         lib.moe_route_expand.argtypes = [_vp, _i64, _int, _int, _int, _vp, _int, _vp, _vp, _vp,
                                          _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
         lib.moe_route_expand.restype = _int
+        lib.moe_route_local_rows.argtypes = [_i64, _int, _int, _int, _int, ctypes.POINTER(_i64)]
+        lib.moe_route_local_rows.restype = _int
+        lib.moe_route_local_workspace_size.argtypes = [_i64, _int, _int, _int, _int,
+                                                       ctypes.POINTER(ctypes.c_size_t)]
+        lib.moe_route_local_workspace_size.restype = _int
+        lib.moe_route_local.argtypes = [_vp, _i64, _int, _int, _int, _int, _int, _int, _vp, _vp, _vp,
+                                        _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        lib.moe_route_local.restype = _int
+        lib.moe_expand_rows.argtypes = [_vp, _i64, _int, _int, _vp, _i64, _vp, _vp]
+        lib.moe_expand_rows.restype = _int
+        lib.moe_combine_rows.argtypes = [_vp, _i64, _i64, _int, _int, _vp, _vp, _vp, _vp]
+        lib.moe_combine_rows.restype = _int
         lib.moe_expand.argtypes = [_vp, _i64, _int, _int, _vp, _vp, _vp]
         lib.moe_expand.restype = _int
         lib.moe_swiglu.argtypes = [_vp, _i64, _int, _vp, _vp]
@@ -254,4 +266,99 @@ def moe_combine(expert_out: torch.Tensor, topk_weights: torch.Tensor, inv_perm: 
     _check("moe_combine", load_library().moe_combine(_ptr(expert_out), T, H, int(k),
                                                      _ptr(topk_weights), _ptr(inv_perm), _ptr(out),
                                                      _stream_ptr(stream, expert_out.device)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# local (one tensor-parallel rank's) routing with padded expert segments
+# ---------------------------------------------------------------------------
+
+def moe_route_local_rows(T: int, k: int, e0: int, e1: int, pad: int) -> int:
+    """Rows of a padded local buffer (perm, expanded_x, expert_out)."""
+    out = _i64(0)
+    _check("moe_route_local_rows",
+           load_library().moe_route_local_rows(int(T), int(k), int(e0), int(e1), int(pad),
+                                               ctypes.byref(out)))
+    return out.value
+
+
+def moe_route_local_workspace_size(T: int, E: int, k: int, e0: int, e1: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("moe_route_local_workspace_size",
+           load_library().moe_route_local_workspace_size(int(T), int(E), int(k), int(e0), int(e1),
+                                                         ctypes.byref(out)))
+    return out.value
+
+
+def moe_route_local(logits: torch.Tensor, k: int, renorm: bool, e0: int, e1: int, pad: int = 1, *,
+                    out: Optional[RouteResult] = None, workspace: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> RouteResult:
+    """Routing of ``logits [T, E]`` for the experts [e0, e1) of one rank,
+    expert segments padded to a multiple of ``pad``. expert_counts has e1-e0
+    entries, expert_offsets e1-e0+1, perm ``moe_route_local_rows(...)`` (-1 on
+    padding rows), inv_perm T*k (-1 for slots of other ranks' experts)."""
+    if logits.dim() != 2:
+        raise ValueError("logits must be [T, E]")
+    T, E = logits.shape
+    _need(logits, "logits", torch.float32, (T, E))
+    dev = logits.device
+    n = e1 - e0
+    rows = moe_route_local_rows(T, k, e0, e1, pad)
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=dev)
+        out = RouteResult(torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev),
+                          torch.empty((n,), **i32), torch.empty((n + 1,), **i32),
+                          torch.empty((rows,), **i32), torch.empty((T * k,), **i32))
+    for name, t, dt, shape in (("topk_ids", out.topk_ids, torch.int32, (T, k)),
+                               ("topk_weights", out.topk_weights, torch.float32, (T, k)),
+                               ("expert_counts", out.expert_counts, torch.int32, (n,)),
+                               ("expert_offsets", out.expert_offsets, torch.int32, (n + 1,)),
+                               ("perm", out.perm, torch.int32, (rows,)),
+                               ("inv_perm", out.inv_perm, torch.int32, (T * k,))):
+        _need(t, name, dt, shape)
+    ws_bytes = moe_route_local_workspace_size(T, E, k, e0, e1)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty((ws_bytes,), dtype=torch.uint8, device=dev)
+    ws_len = 0 if workspace is None else workspace.numel()
+    st = load_library().moe_route_local(_ptr(logits), T, E, int(k), int(bool(renorm)), int(e0), int(e1),
+                                        int(pad), _ptr(out.topk_ids), _ptr(out.topk_weights),
+                                        _ptr(out.expert_counts), _ptr(out.expert_offsets),
+                                        _ptr(out.perm), _ptr(out.inv_perm), _ptr(workspace), ws_len,
+                                        _stream_ptr(stream, dev))
+    _check("moe_route_local", st)
+    return out
+
+
+def moe_expand_rows(x: torch.Tensor, inv_perm: torch.Tensor, k: int, rows: int, *,
+                    out: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """moe_expand into ``rows`` rows; inv_perm entries outside [0, rows) are
+    skipped and rows nothing maps to are left as they are."""
+    T, H = x.shape
+    _need(x, "x", torch.bfloat16, (T, H))
+    _need(inv_perm, "inv_perm", torch.int32, (T * k,))
+    if out is None:
+        out = torch.empty((rows, H), dtype=torch.bfloat16, device=x.device)
+    _need(out, "expanded_x", torch.bfloat16, (rows, H))
+    _check("moe_expand_rows", load_library().moe_expand_rows(_ptr(x), T, H, int(k), _ptr(inv_perm), rows,
+                                                             _ptr(out), _stream_ptr(stream, x.device)))
+    return out
+
+
+def moe_combine_rows(expert_out: torch.Tensor, topk_weights: torch.Tensor, inv_perm: torch.Tensor, *,
+                     out: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """moe_combine over an expert_out of any number of rows; inv_perm entries
+    outside [0, rows) contribute nothing (a rank's partial sum)."""
+    T, k = topk_weights.shape
+    rows, H = expert_out.shape
+    _need(expert_out, "expert_out", torch.bfloat16, (rows, H))
+    _need(topk_weights, "topk_weights", torch.float32, (T, k))
+    _need(inv_perm, "inv_perm", torch.int32, (T * k,))
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=expert_out.device)
+    _need(out, "out", torch.bfloat16, (T, H))
+    _check("moe_combine_rows", load_library().moe_combine_rows(_ptr(expert_out), rows, T, H, int(k),
+                                                               _ptr(topk_weights), _ptr(inv_perm), _ptr(out),
+                                                               _stream_ptr(stream, expert_out.device)))
     return out

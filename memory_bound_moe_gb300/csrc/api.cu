@@ -75,6 +75,17 @@ moe_status_t check_rows(int64_t rows, int width, int64_t slots_mult) {
 
 moe_status_t from_cuda(cudaError_t err) { return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Local routing arguments: 0 <= e0 < e1 <= E, pad >= 1, padded capacity < 2^31.
+moe_status_t check_local(int64_t T, int E, int k, int e0, int e1, int pad, int64_t* rows) {
+    moe_status_t st = check_route_sizes(T, E, k);
+    if (st != MOE_OK) return st;
+    if (e0 < 0 || e1 > E || e0 >= e1 || pad < 1) return MOE_ERR_INVALID_ARG;
+    const int64_t r = T * int64_t(k) + int64_t(e1 - e0) * int64_t(pad - 1);
+    if (r >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (rows) *rows = r;
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -191,6 +202,116 @@ moe_status_t moe_route_expand(const float* logits, int64_t T, int E, int k, int 
     return moe_expand(x, T, H, k, inv_perm, expanded_x, stream);
 }
 
+moe_status_t moe_route_local_rows(int64_t T, int k, int e0, int e1, int pad, int64_t* rows) {
+    if (rows == nullptr || T < 0 || k < 1 || e0 < 0 || e0 >= e1 || pad < 1) return MOE_ERR_INVALID_ARG;
+    const int64_t r = T * int64_t(k) + int64_t(e1 - e0) * int64_t(pad - 1);
+    if (r >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    *rows = r;
+    return MOE_OK;
+}
+
+moe_status_t moe_route_local_workspace_size(int64_t T, int E, int k, int e0, int e1, size_t* bytes) {
+    if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+    const moe_status_t st = check_local(T, E, k, e0, e1, 1, nullptr);
+    if (st != MOE_OK) return st;
+    *bytes = T == 0 ? 0 : moe::plan_route(T, E, k, e1 - e0).ws_bytes;
+    return MOE_OK;
+}
+
+moe_status_t moe_route_local(const float* logits, int64_t T, int E, int k, int renorm, int e0,
+                             int e1, int pad, int32_t* topk_ids, float* topk_weights,
+                             int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
+                             int32_t* inv_perm, void* workspace, size_t workspace_bytes,
+                             moe_stream_t stream) {
+    int64_t rows = 0;
+    moe_status_t st = check_local(T, E, k, e0, e1, pad, &rows);
+    if (st != MOE_OK) return st;
+    const int n = e1 - e0;
+    if (expert_counts == nullptr || expert_offsets == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned4(expert_counts) || !aligned4(expert_offsets)) return MOE_ERR_MISALIGNED;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        if (any_overlap({{expert_counts, 4ull * n}, {expert_offsets, 4ull * (n + 1)}, {perm, 4ull * rows}}, {}))
+            return MOE_ERR_INVALID_ARG;
+        cudaError_t err = cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * n, s);
+        if (err == cudaSuccess) err = cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (n + 1), s);
+        if (err == cudaSuccess && rows > 0) {
+            if (perm == nullptr) return MOE_ERR_INVALID_ARG;
+            err = cudaMemsetAsync(perm, 0xff, sizeof(int32_t) * rows, s);   // all -1
+        }
+        return from_cuda(err);
+    }
+    if (logits == nullptr || topk_ids == nullptr || topk_weights == nullptr || perm == nullptr ||
+        inv_perm == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned4(logits) || !aligned4(topk_ids) || !aligned4(topk_weights) || !aligned4(perm) ||
+        !aligned4(inv_perm))
+        return MOE_ERR_MISALIGNED;
+    const moe::RoutePlan plan = moe::plan_route(T, E, k, n);
+    if (plan.ws_bytes > 0) {
+        if (workspace == nullptr || workspace_bytes < plan.ws_bytes) return MOE_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return MOE_ERR_MISALIGNED;
+    }
+    const uint64_t S = uint64_t(T) * uint64_t(k);
+    if (any_overlap({{topk_ids, 4 * S}, {topk_weights, 4 * S}, {expert_counts, 4ull * n},
+                     {expert_offsets, 4ull * (n + 1)}, {perm, 4ull * rows}, {inv_perm, 4 * S},
+                     {workspace, plan.ws_bytes}},
+                    {{logits, 4ull * uint64_t(T) * E}}))
+        return MOE_ERR_INVALID_ARG;
+    const moe::LocalRange local{e0, n, pad, int(rows)};
+    return from_cuda(moe::launch_route(plan, logits, int(T), E, k, renorm ? 1 : 0, topk_ids,
+                                       topk_weights, expert_counts, expert_offsets, perm, inv_perm,
+                                       workspace, s, &local));
+}
+
+moe_status_t moe_expand_rows(const moe_bf16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
+                             int64_t rows, moe_bf16_t* expanded_x, moe_stream_t stream) {
+    if (k < 1) return MOE_ERR_INVALID_ARG;
+    if (k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
+    moe_status_t st = check_rows(T, H, k);
+    if (st != MOE_OK) return st;
+    if (rows < 0) return MOE_ERR_INVALID_ARG;
+    if (rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (T == 0 || rows == 0) return MOE_OK;
+    if (x == nullptr || inv_perm == nullptr || expanded_x == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(expanded_x) || !aligned4(inv_perm)) return MOE_ERR_MISALIGNED;
+    const uint64_t S = uint64_t(T) * uint64_t(k);
+    if (any_overlap({{expanded_x, 2 * uint64_t(rows) * uint64_t(H)}},
+                    {{x, 2 * uint64_t(T) * uint64_t(H)}, {inv_perm, 4 * S}}))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_expand(x, T, H, k, inv_perm, rows, expanded_x, sms,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_combine_rows(const moe_bf16_t* expert_out, int64_t rows, int64_t T, int H, int k,
+                              const float* topk_weights, const int32_t* inv_perm, moe_bf16_t* out,
+                              moe_stream_t stream) {
+    if (k < 1) return MOE_ERR_INVALID_ARG;
+    if (k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
+    moe_status_t st = check_rows(T, H, k);
+    if (st != MOE_OK) return st;
+    if (rows < 0) return MOE_ERR_INVALID_ARG;
+    if (rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (topk_weights == nullptr || inv_perm == nullptr || out == nullptr ||
+        (rows > 0 && expert_out == nullptr))
+        return MOE_ERR_INVALID_ARG;
+    if ((rows > 0 && !aligned16(expert_out)) || !aligned16(out) || !aligned4(topk_weights) ||
+        !aligned4(inv_perm))
+        return MOE_ERR_MISALIGNED;
+    const uint64_t S = uint64_t(T) * uint64_t(k);
+    if (any_overlap({{out, 2 * uint64_t(T) * uint64_t(H)}},
+                    {{expert_out, 2 * uint64_t(rows) * uint64_t(H)}, {topk_weights, 4 * S},
+                     {inv_perm, 4 * S}}))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_combine(expert_out, rows, T, H, k, topk_weights, inv_perm, out, sms,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_expand(const moe_bf16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
                         moe_bf16_t* expanded_x, moe_stream_t stream) {
     if (k < 1) return MOE_ERR_INVALID_ARG;
@@ -207,7 +328,7 @@ moe_status_t moe_expand(const moe_bf16_t* x, int64_t T, int H, int k, const int3
     int sms = 0;
     cudaError_t err = current_sm_count(&sms);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    return from_cuda(moe::launch_expand(x, T, H, k, inv_perm, expanded_x, sms,
+    return from_cuda(moe::launch_expand(x, T, H, k, inv_perm, T * k, expanded_x, sms,
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -248,7 +369,7 @@ moe_status_t moe_combine(const moe_bf16_t* expert_out, int64_t T, int H, int k,
     int sms = 0;
     cudaError_t err = current_sm_count(&sms);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    return from_cuda(moe::launch_combine(expert_out, T, H, k, topk_weights, inv_perm, out, sms,
+    return from_cuda(moe::launch_combine(expert_out, T * k, T, H, k, topk_weights, inv_perm, out, sms,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -96,12 +96,12 @@ __global__ void __launch_bounds__(NT) combine_kernel(const uint8_t* __restrict__
 constexpr int kNt = MOE_COMBINE_NT;
 
 template <int VB, int KT>
-cudaError_t launch_t(const uint16_t* eo, int64_t T, int H, int k, const float* w,
+cudaError_t launch_t(const uint16_t* eo, int64_t rows, int64_t T, int H, int k, const float* w,
                      const int32_t* inv_perm, uint16_t* out, int num_sms, cudaStream_t stream) {
     auto kernel = combine_kernel<VB, KT, kNt>;
     static const int occ = resident_blocks(kernel, kNt);
     const uint32_t nv = uint32_t(uint64_t(H) * 2 / VB);
-    const uint32_t S = uint32_t(T * k);
+    const uint32_t S = uint32_t(rows);
     const int64_t tok_per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / nv));
     for (int64_t t0 = 0; t0 < T; t0 += tok_per_launch) {
         const int64_t nt = std::min(tok_per_launch, T - t0);
@@ -117,27 +117,27 @@ cudaError_t launch_t(const uint16_t* eo, int64_t T, int H, int k, const float* w
 }
 
 template <int VB>
-cudaError_t launch_vb(const uint16_t* eo, int64_t T, int H, int k, const float* w,
+cudaError_t launch_vb(const uint16_t* eo, int64_t rows, int64_t T, int H, int k, const float* w,
                       const int32_t* inv_perm, uint16_t* out, int num_sms, cudaStream_t stream) {
     switch (k) {
-        case 1: return launch_t<VB, 1>(eo, T, H, k, w, inv_perm, out, num_sms, stream);
-        case 2: return launch_t<VB, 2>(eo, T, H, k, w, inv_perm, out, num_sms, stream);
-        case 4: return launch_t<VB, 4>(eo, T, H, k, w, inv_perm, out, num_sms, stream);
-        case 8: return launch_t<VB, 8>(eo, T, H, k, w, inv_perm, out, num_sms, stream);
-        default: return launch_t<VB, 0>(eo, T, H, k, w, inv_perm, out, num_sms, stream);
+        case 1: return launch_t<VB, 1>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        case 2: return launch_t<VB, 2>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        case 4: return launch_t<VB, 4>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        case 8: return launch_t<VB, 8>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        default: return launch_t<VB, 0>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_combine(const uint16_t* expert_out, int64_t T, int H, int k,
+cudaError_t launch_combine(const uint16_t* expert_out, int64_t rows, int64_t T, int H, int k,
                            const float* topk_weights, const int32_t* inv_perm, uint16_t* out,
                            int num_sms, cudaStream_t stream) {
     // 8 gathered rows of 32 bytes would hold 64 registers of loads per thread;
     // large k keeps 16-byte vectors (still k loads in flight).
     if (k < MOE_COMBINE_WIDE_BELOW_K && can_use_32b(uint64_t(H) * 2, {expert_out, out}))
-        return launch_vb<32>(expert_out, T, H, k, topk_weights, inv_perm, out, num_sms, stream);
-    return launch_vb<16>(expert_out, T, H, k, topk_weights, inv_perm, out, num_sms, stream);
+        return launch_vb<32>(expert_out, rows, T, H, k, topk_weights, inv_perm, out, num_sms, stream);
+    return launch_vb<16>(expert_out, rows, T, H, k, topk_weights, inv_perm, out, num_sms, stream);
 }
 
 }  // namespace moe

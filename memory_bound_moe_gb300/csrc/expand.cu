@@ -62,11 +62,11 @@ constexpr int kUnroll = MOE_EXPAND_UNROLL;
 
 template <int VB>
 cudaError_t launch_vb(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
-                      uint16_t* out, int num_sms, cudaStream_t stream) {
+                      int64_t rows, uint16_t* out, int num_sms, cudaStream_t stream) {
     auto kernel = expand_kernel<VB, kUnroll, kNt>;
     static const int occ = resident_blocks(kernel, kNt);
     const uint32_t nv = uint32_t(uint64_t(H) * 2 / VB);
-    const uint32_t S = uint32_t(T * k);
+    const uint32_t S = uint32_t(rows);
     const int64_t tok_per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / nv));
     for (int64_t t0 = 0; t0 < T; t0 += tok_per_launch) {
         const int64_t nt = std::min(tok_per_launch, T - t0);
@@ -84,10 +84,10 @@ cudaError_t launch_vb(const uint16_t* x, int64_t T, int H, int k, const int32_t*
 }  // namespace
 
 cudaError_t launch_expand(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
-                          uint16_t* expanded_x, int num_sms, cudaStream_t stream) {
+                          int64_t rows, uint16_t* expanded_x, int num_sms, cudaStream_t stream) {
     if (can_use_32b(uint64_t(H) * 2, {x, expanded_x}))
-        return launch_vb<32>(x, T, H, k, inv_perm, expanded_x, num_sms, stream);
-    return launch_vb<16>(x, T, H, k, inv_perm, expanded_x, num_sms, stream);
+        return launch_vb<32>(x, T, H, k, inv_perm, rows, expanded_x, num_sms, stream);
+    return launch_vb<16>(x, T, H, k, inv_perm, rows, expanded_x, num_sms, stream);
 }
 
 }  // namespace moe

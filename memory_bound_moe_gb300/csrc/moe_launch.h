@@ -24,12 +24,20 @@ struct RoutePlan {
     size_t smem_scatter = 0;
 };
 
-RoutePlan plan_route(int64_t T, int E, int k);
+// nloc: number of counted experts (0 = all E); it sets the count-matrix width.
+RoutePlan plan_route(int64_t T, int E, int k, int nloc = 0);
+
+// A local routing: experts [e0, e0 + n) are counted, their segments padded
+// to a multiple of pad, perm has `rows` entries.
+struct LocalRange {
+    int e0, n, pad, rows;
+};
 
 cudaError_t launch_route(const RoutePlan& plan, const float* logits, int T, int E, int k,
                          int renorm, int32_t* topk_ids, float* topk_weights,
                          int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
-                         int32_t* inv_perm, void* workspace, cudaStream_t stream);
+                         int32_t* inv_perm, void* workspace, cudaStream_t stream,
+                         const LocalRange* local = nullptr);
 
 // One-launch route + expand for decode-sized batches (route_expand.cu).
 bool route_expand_fits(const RoutePlan& plan);
@@ -39,13 +47,16 @@ cudaError_t launch_route_expand(const RoutePlan& plan, const float* logits, int 
                                 int32_t* inv_perm, const uint16_t* x, int H, uint16_t* expanded_x,
                                 int num_sms, cudaStream_t stream);
 
+// rows: rows of expanded_x (T*k, or a padded local capacity); inv_perm
+// entries outside [0, rows) are skipped.
 cudaError_t launch_expand(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
-                          uint16_t* expanded_x, int num_sms, cudaStream_t stream);
+                          int64_t rows, uint16_t* expanded_x, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_swiglu(const uint16_t* gate_up, int64_t rows, int I, uint16_t* act,
                           int num_sms, cudaStream_t stream);
 
-cudaError_t launch_combine(const uint16_t* expert_out, int64_t T, int H, int k,
+// rows: rows of expert_out; inv_perm entries outside [0, rows) contribute nothing.
+cudaError_t launch_combine(const uint16_t* expert_out, int64_t rows, int64_t T, int H, int k,
                            const float* topk_weights, const int32_t* inv_perm, uint16_t* out,
                            int num_sms, cudaStream_t stream);
 

@@ -39,26 +39,26 @@
 namespace moe {
 namespace {
 
-template <int GS, int EPL, int NT>
+template <int GS, int EPL, int NT, bool LOCAL>
 __global__ void __launch_bounds__(NT) route_rank_kernel(RouteArgs a) {
     constexpr int NW = NT / kWarp;
     extern __shared__ int32_t smem[];
-    int32_t* s_cnt = smem;                      // [NW][E]
-    int32_t* s_tot = s_cnt + (size_t)NW * a.E;  // [Ep]
+    int32_t* s_cnt = smem;                         // [NW][nloc]
+    int32_t* s_tot = s_cnt + (size_t)NW * a.nloc;  // [Ep]
     pdl_wait_and_release();
-    for (int i = threadIdx.x; i < NW * a.E; i += NT) s_cnt[i] = 0;
+    for (int i = threadIdx.x; i < NW * a.nloc; i += NT) s_cnt[i] = 0;
     for (int e = threadIdx.x; e < a.Ep; e += NT) s_tot[e] = 0;
     __syncthreads();
     const int t0 = blockIdx.x * a.tpc;
     const int t1 = min(a.T, t0 + a.tpc);
     int re[kRegRounds], rr[kRegRounds];
-    topk_rank_range<GS, EPL, NT>(a, t0, t1, s_cnt, re, rr);
+    topk_rank_range<GS, EPL, NT, LOCAL>(a, t0, t1, s_cnt, re, rr);
     __syncthreads();
-    scan_over_warps<NT>(s_cnt, s_tot, a.E);
+    scan_over_warps<NT>(s_cnt, s_tot, a.nloc);
     __syncthreads();
     int32_t* row = a.ws_counts + (size_t)blockIdx.x * a.Ep;
     for (int e = threadIdx.x; e < a.Ep; e += NT) row[e] = s_tot[e];
-    finish_ranks<GS, NT, false>(a, t0, t1, s_cnt, nullptr, re, rr);
+    finish_ranks<GS, NT, false, LOCAL>(a, t0, t1, s_cnt, nullptr, re, rr);
 }
 
 // Number of row groups the place kernel splits the count matrix into.
@@ -67,7 +67,39 @@ __host__ __device__ inline int place_rowgroups(int Ep, int nt) {
     return cg >= nt ? 1 : nt / cg;
 }
 
+// Offsets from the block's expert totals s_tot[0..nloc): the exclusive scan
+// of the counts, each rounded up to a multiple of pad for a local routing.
+// Writes s_off[0..nloc] (s_off[nloc] = total rows used) and, when `out`,
+// expert_counts and expert_offsets. Block-wide; returns the total.
+template <int NT, bool LOCAL>
+__device__ __forceinline__ int compute_offsets(const RouteArgs& a, const int32_t* s_tot, int32_t* s_off,
+                                              int32_t* s_warp, bool out) {
+    for (int e = threadIdx.x; e < a.nloc; e += NT) {
+        const int c = s_tot[e];
+        if (out) a.expert_counts[e] = c;
+        s_off[e] = LOCAL ? (c + a.pad - 1) / a.pad * a.pad : c;
+    }
+    __syncthreads();
+    const int total = block_exclusive_scan<NT>(s_off, s_off, a.nloc, s_warp);
+    if (threadIdx.x == 0) s_off[a.nloc] = total;
+    for (int e = threadIdx.x; e < a.nloc; e += NT)
+        if (out) a.expert_offsets[e] = s_off[e];
+    if (out && threadIdx.x == 0) a.expert_offsets[a.nloc] = total;
+    __syncthreads();
+    return total;
+}
+
+// perm = -1 on the padding rows of local experts l = l0, l0 + dl, ... and on
+// the rows [total + r0, rows) in steps of dr (block-strided by the caller).
 template <int NT>
+__device__ __forceinline__ void fill_padding(const RouteArgs& a, const int32_t* s_tot, const int32_t* s_off,
+                                             int l0, int dl, int r0, int dr) {
+    for (int l = l0; l < a.nloc; l += dl)
+        for (int q = s_off[l] + s_tot[l] + threadIdx.x; q < s_off[l + 1]; q += NT) a.perm[q] = -1;
+    for (int q = s_off[a.nloc] + r0 + threadIdx.x; q < a.rows; q += dr) a.perm[q] = -1;
+}
+
+template <int NT, bool LOCAL>
 __global__ void __launch_bounds__(NT) route_place_kernel(RouteArgs a) {
     extern __shared__ int32_t smem[];
     const int Ep = a.Ep;
@@ -77,7 +109,8 @@ __global__ void __launch_bounds__(NT) route_place_kernel(RouteArgs a) {
     int32_t* s_ppre = s_ptot + R * Ep;      // [R][Ep]
     int32_t* s_tot = s_ppre + R * Ep;       // [Ep]
     int32_t* s_base = s_tot + Ep;           // [Ep]
-    int32_t* s_warp = s_base + Ep;          // [32]
+    int32_t* s_off = s_base + Ep;           // [Ep + 4]
+    int32_t* s_warp = s_off + Ep + 4;       // [32]
     const int b = blockIdx.x;
     pdl_wait_and_release();
 
@@ -114,47 +147,44 @@ __global__ void __launch_bounds__(NT) route_place_kernel(RouteArgs a) {
         s_base[c] = pre;
     }
     __syncthreads();
-    if (b == 0) {
-        for (int e = threadIdx.x; e < a.E; e += NT) a.expert_counts[e] = s_tot[e];
-    }
-    block_exclusive_scan<NT>(s_tot, s_tot, a.E, s_warp);   // s_tot := offsets
-    for (int e = threadIdx.x; e < a.E; e += NT) {
-        if (b == 0) a.expert_offsets[e] = s_tot[e];
-        s_base[e] += s_tot[e];
-    }
-    if (b == 0 && threadIdx.x == 0) a.expert_offsets[a.E] = a.T * a.k;
+    compute_offsets<NT, LOCAL>(a, s_tot, s_off, s_warp, b == 0);
+    for (int e = threadIdx.x; e < a.nloc; e += NT) s_base[e] += s_off[e];
     __syncthreads();
 
     const int s0 = b * a.tpc * a.k;
     const int s1 = min(a.T, (b + 1) * a.tpc) * a.k;
     for (int s = s0 + threadIdx.x; s < s1; s += NT) {
-        const int e = __ldcg(a.topk_ids + s);
+        int e = __ldcg(a.topk_ids + s);
+        if constexpr (LOCAL) {
+            e -= a.e0;
+            if (e < 0 || e >= a.nloc) continue;   // inv_perm already -1
+        }
         const int p = s_base[e] + __ldcg(a.inv_perm + s);
         a.perm[p] = s;
         a.inv_perm[s] = p;
     }
+    if constexpr (LOCAL) fill_padding<NT>(a, s_tot, s_off, b, a.G, b * NT, a.G * NT);
 }
 
-template <int GS, int EPL, int NT>
+template <int GS, int EPL, int NT, bool LOCAL>
 __global__ void __launch_bounds__(NT) route_fused_kernel(RouteArgs a) {
     constexpr int NW = NT / kWarp;
     extern __shared__ int32_t smem[];
-    int32_t* s_cnt = smem;                      // [NW][E]
-    int32_t* s_tot = s_cnt + (size_t)NW * a.E;  // [Ep] totals, then offsets
-    int32_t* s_warp = s_tot + a.Ep;             // [32]
+    int32_t* s_cnt = smem;                         // [NW][nloc]
+    int32_t* s_tot = s_cnt + (size_t)NW * a.nloc;  // [Ep] totals
+    int32_t* s_off = s_tot + a.Ep;                 // [Ep + 4] offsets
+    int32_t* s_warp = s_off + a.Ep + 4;            // [32]
     pdl_wait_and_release();
-    for (int i = threadIdx.x; i < NW * a.E; i += NT) s_cnt[i] = 0;
+    for (int i = threadIdx.x; i < NW * a.nloc; i += NT) s_cnt[i] = 0;
     __syncthreads();
     int re[kRegRounds], rr[kRegRounds];
-    topk_rank_range<GS, EPL, NT>(a, 0, a.T, s_cnt, re, rr);
+    topk_rank_range<GS, EPL, NT, LOCAL>(a, 0, a.T, s_cnt, re, rr);
     __syncthreads();
-    scan_over_warps<NT>(s_cnt, s_tot, a.E);
+    scan_over_warps<NT>(s_cnt, s_tot, a.nloc);
     __syncthreads();
-    for (int e = threadIdx.x; e < a.E; e += NT) a.expert_counts[e] = s_tot[e];
-    block_exclusive_scan<NT>(s_tot, s_tot, a.E, s_warp);
-    for (int e = threadIdx.x; e < a.E; e += NT) a.expert_offsets[e] = s_tot[e];
-    if (threadIdx.x == 0) a.expert_offsets[a.E] = a.T * a.k;
-    finish_ranks<GS, NT, true>(a, 0, a.T, s_cnt, s_tot, re, rr);
+    compute_offsets<NT, LOCAL>(a, s_tot, s_off, s_warp, true);
+    finish_ranks<GS, NT, true, LOCAL>(a, 0, a.T, s_cnt, s_off, re, rr);
+    if constexpr (LOCAL) fill_padding<NT>(a, s_tot, s_off, 0, 1, 0, NT);
 }
 
 #ifndef MOE_ROUTE_NT
@@ -175,16 +205,16 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
 }
 
-template <int GS, int EPL>
+template <int GS, int EPL, bool LOCAL>
 cudaError_t launch_route_t(const RoutePlan& p, const RouteArgs& a, cudaStream_t stream) {
     cudaError_t err;
     if (p.fused) {
-        auto kf = route_fused_kernel<GS, EPL, kNtFused>;
+        auto kf = route_fused_kernel<GS, EPL, kNtFused, LOCAL>;
         if ((err = allow_smem(kf, p.smem_topk)) != cudaSuccess) return err;
         return launch_pdl(kf, dim3(1), dim3(kNtFused), p.smem_topk, stream, a);
     }
-    auto k1 = route_rank_kernel<GS, EPL, kNtSplit>;
-    auto k2 = route_place_kernel<kNtSplit>;
+    auto k1 = route_rank_kernel<GS, EPL, kNtSplit, LOCAL>;
+    auto k2 = route_place_kernel<kNtSplit, LOCAL>;
     if ((err = allow_smem(k1, p.smem_topk)) != cudaSuccess) return err;
     if ((err = allow_smem(k2, p.smem_scatter)) != cudaSuccess) return err;
     if ((err = launch_pdl(k1, dim3(p.G), dim3(kNtSplit), p.smem_topk, stream, a)) != cudaSuccess)
@@ -192,16 +222,32 @@ cudaError_t launch_route_t(const RoutePlan& p, const RouteArgs& a, cudaStream_t 
     return launch_pdl(k2, dim3(p.G), dim3(kNtSplit), p.smem_scatter, stream, a);
 }
 
+template <bool LOCAL>
+cudaError_t launch_route_local(const RoutePlan& plan, const RouteArgs& a, cudaStream_t stream) {
+    switch (plan.gs * 100 + plan.epl) {
+        case 801: return launch_route_t<8, 1, LOCAL>(plan, a, stream);
+        case 1601: return launch_route_t<16, 1, LOCAL>(plan, a, stream);
+        case 3201: return launch_route_t<32, 1, LOCAL>(plan, a, stream);
+        case 3202: return launch_route_t<32, 2, LOCAL>(plan, a, stream);
+        case 3204: return launch_route_t<32, 4, LOCAL>(plan, a, stream);
+        case 3208: return launch_route_t<32, 8, LOCAL>(plan, a, stream);
+        case 3216: return launch_route_t<32, 16, LOCAL>(plan, a, stream);
+        case 3232: return launch_route_t<32, 32, LOCAL>(plan, a, stream);
+        default: return cudaErrorInvalidConfiguration;
+    }
+}
+
 }  // namespace
 
-RoutePlan plan_route(int64_t T, int E, int k) {
+RoutePlan plan_route(int64_t T, int E, int k, int nloc) {
     (void)k;
+    if (nloc <= 0) nloc = E;
     RoutePlan p;
     if (E <= 8) { p.gs = 8; p.epl = 1; }
     else if (E <= 16) { p.gs = 16; p.epl = 1; }
     else { p.gs = 32; p.epl = (E + 31) / 32; }
     if (p.epl > 2) p.epl = p.epl <= 4 ? 4 : p.epl <= 8 ? 8 : p.epl <= 16 ? 16 : 32;
-    p.Ep = (E + 3) / 4 * 4;
+    p.Ep = (nloc + 3) / 4 * 4;
     const int gpw = kWarp / p.gs;
     const int fused_groups = (kNtFused / kWarp) * gpw;
     p.fused = T <= 2 * fused_groups;
@@ -212,7 +258,7 @@ RoutePlan plan_route(int64_t T, int E, int k) {
         p.tpc = int(T);
         p.tpw = int(((T + nw - 1) / nw + gpw - 1) / gpw * gpw);
         p.ws_bytes = 0;
-        p.smem_topk = sizeof(int32_t) * (size_t(nw) * E + p.Ep + 32);
+        p.smem_topk = sizeof(int32_t) * (size_t(nw) * nloc + 2 * size_t(p.Ep) + 4 + 32);
         return p;
     }
     const int nw = kNtSplit / kWarp;
@@ -224,36 +270,31 @@ RoutePlan plan_route(int64_t T, int E, int k) {
     p.tpw = int(((tpc + nw - 1) / nw + gpw - 1) / gpw * gpw);
     p.G = int((T + tpc - 1) / tpc);
     p.ws_bytes = sizeof(int32_t) * size_t(p.G) * size_t(p.Ep);
-    p.smem_topk = sizeof(int32_t) * (size_t(nw) * E + p.Ep);
+    p.smem_topk = sizeof(int32_t) * (size_t(nw) * nloc + p.Ep);
     const int R = place_rowgroups(p.Ep, kNtSplit);
-    p.smem_scatter = sizeof(int32_t) * (size_t(2) * R * p.Ep + 2 * size_t(p.Ep) + 32);
+    p.smem_scatter = sizeof(int32_t) * (size_t(2) * R * p.Ep + 3 * size_t(p.Ep) + 4 + 32);
     return p;
 }
 
 cudaError_t launch_route(const RoutePlan& plan, const float* logits, int T, int E, int k,
                          int renorm, int32_t* topk_ids, float* topk_weights,
                          int32_t* expert_counts, int32_t* expert_offsets, int32_t* perm,
-                         int32_t* inv_perm, void* workspace, cudaStream_t stream) {
+                         int32_t* inv_perm, void* workspace, cudaStream_t stream,
+                         const LocalRange* local) {
     RouteArgs a;
     a.logits = logits;
     a.T = T; a.E = E; a.k = k; a.renorm = renorm;
+    a.e0 = local ? local->e0 : 0;
+    a.nloc = local ? local->n : E;
+    a.pad = local ? local->pad : 1;
+    a.rows = local ? local->rows : T * k;
     a.Ep = plan.Ep; a.tpc = plan.tpc; a.tpw = plan.tpw; a.G = plan.G;
     a.topk_ids = topk_ids; a.topk_weights = topk_weights;
     a.expert_counts = expert_counts; a.expert_offsets = expert_offsets;
     a.perm = perm; a.inv_perm = inv_perm;
     a.ws_counts = static_cast<int32_t*>(workspace);
     a.write_out = true;
-    switch (plan.gs * 100 + plan.epl) {
-        case 801: return launch_route_t<8, 1>(plan, a, stream);
-        case 1601: return launch_route_t<16, 1>(plan, a, stream);
-        case 3201: return launch_route_t<32, 1>(plan, a, stream);
-        case 3202: return launch_route_t<32, 2>(plan, a, stream);
-        case 3204: return launch_route_t<32, 4>(plan, a, stream);
-        case 3208: return launch_route_t<32, 8>(plan, a, stream);
-        case 3216: return launch_route_t<32, 16>(plan, a, stream);
-        case 3232: return launch_route_t<32, 32>(plan, a, stream);
-        default: return cudaErrorInvalidConfiguration;
-    }
+    return local ? launch_route_local<true>(plan, a, stream) : launch_route_local<false>(plan, a, stream);
 }
 
 }  // namespace moe

@@ -13,7 +13,10 @@ namespace moe {
 struct RouteArgs {
     const float* logits;
     int T, E, k, renorm;
-    int Ep;    // count-matrix row stride (E rounded up to 4)
+    int e0, nloc;  // counted experts: [e0, e0 + nloc) (all E unless a local routing)
+    int pad;       // expert segments rounded up to a multiple of pad (local routing)
+    int rows;      // entries of perm (T*k, or the padded capacity of a local routing)
+    int Ep;    // count-matrix row stride (nloc rounded up to 4)
     int tpc;   // tokens per block
     int tpw;   // tokens per warp (a multiple of the token groups per warp)
     int G;     // blocks
@@ -153,14 +156,15 @@ __device__ __forceinline__ int topk_select(const RouteArgs& a, int t, bool valid
 constexpr int kRegRounds = 4;
 
 // Top-k of the tokens [t0, t1) and the rank of every slot among this warp's
-// slots of the same expert; s_cnt is [NW][E] and counts each warp's picks per
-// expert. Warp w owns tokens [t0 + w*tpw, t0 + (w+1)*tpw); each round takes
-// GPW consecutive tokens, one per lane group, so lane order within a round
-// is slot order. The first kRegRounds rounds return each lane's expert and
-// rank in re/rr (expert -1: no slot); the rank of later rounds is written to
-// inv_perm[s]. The next round's logits are loaded before the current round's
-// selection.
-template <int GS, int EPL, int NT>
+// slots of the same expert; s_cnt is [NW][nloc] and counts each warp's picks
+// per counted expert. Warp w owns tokens [t0 + w*tpw, t0 + (w+1)*tpw); each
+// round takes GPW consecutive tokens, one per lane group, so lane order
+// within a round is slot order. The first kRegRounds rounds return each
+// lane's counted expert and rank in re/rr (re: -1 no slot, -2 a slot whose
+// expert is not counted); the rank of later rounds is written to inv_perm[s]
+// (-1 for uncounted slots). The next round's logits are loaded before the
+// current round's selection. LOCAL counts only experts [e0, e0 + nloc).
+template <int GS, int EPL, int NT, bool LOCAL = false>
 __device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int t1, int32_t* s_cnt,
                                                 int (&re)[kRegRounds], int (&rr)[kRegRounds]) {
     constexpr int GPW = kWarp / GS;
@@ -169,9 +173,13 @@ __device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int 
     const int grp = lane / GS;
     const int gl = lane % GS;
     const unsigned lower = (1u << lane) - 1u;
-    int32_t* cnt = s_cnt + (size_t)warp * a.E;
+    int32_t* cnt = s_cnt + (size_t)warp * a.nloc;
     const int w0 = t0 + warp * a.tpw;
     const int w1 = min(t1, w0 + a.tpw);
+    auto counted = [&](int e) {
+        if constexpr (LOCAL) return (e < 0) ? -1 : (e >= a.e0 && e < a.e0 + a.nloc) ? e - a.e0 : -2;
+        else return e;
+    };
 
     uint32_t key[EPL], next[EPL];
     load_keys<GS, EPL>(a, w0 + grp, w0 + grp < w1, gl, key);
@@ -184,7 +192,7 @@ __device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int 
             const int tn = tb + GPW + grp;
             load_keys<GS, EPL>(a, tn, tn < w1, gl, next);
             const int t = tb + grp;
-            const int e = topk_select<GS, EPL>(a, t, t < w1, gl, key);
+            const int e = counted(topk_select<GS, EPL>(a, t, t < w1, gl, key));
             const unsigned peers = __match_any_sync(kFull, e);
             re[r] = e;
             rr[r] = (e >= 0) ? cnt[e] + __popc(peers & lower) : 0;
@@ -197,11 +205,12 @@ __device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int 
     }
     for (int tb = w0 + kRegRounds * GPW; tb < w1; tb += GPW) {
         const int t = tb + grp;
-        const int e = topk_select<GS, EPL>(a, t, t < w1, gl, key);
+        const int e = counted(topk_select<GS, EPL>(a, t, t < w1, gl, key));
         const int tn = tb + GPW + grp;
         load_keys<GS, EPL>(a, tn, tn < w1, gl, key);
         const unsigned peers = __match_any_sync(kFull, e);
         if (e >= 0) a.inv_perm[(size_t)t * a.k + gl] = cnt[e] + __popc(peers & lower);
+        if (e == -2) a.inv_perm[(size_t)t * a.k + gl] = -1;
         __syncwarp();
         if (e >= 0 && lane == __ffs(peers) - 1) cnt[e] += __popc(peers);
         __syncwarp();
@@ -226,9 +235,9 @@ __device__ __forceinline__ void scan_over_warps(int32_t* s_cnt, int32_t* s_tot, 
 }
 
 // Exclusive scan of in[0..n) into out[0..n) (may alias) by a block of NT
-// threads, n <= MOE_MAX_EXPERTS. Uses s_warp[32].
+// threads, n <= MOE_MAX_EXPERTS; returns the total. Uses s_warp[32].
 template <int NT>
-__device__ void block_exclusive_scan(const int32_t* in, int32_t* out, int n, int32_t* s_warp) {
+__device__ int block_exclusive_scan(const int32_t* in, int32_t* out, int n, int32_t* s_warp) {
     constexpr int ITEMS = (1024 + NT - 1) / NT;
     constexpr int NW = NT / kWarp;
     const int lane = threadIdx.x % kWarp;
@@ -265,14 +274,17 @@ __device__ void block_exclusive_scan(const int32_t* in, int32_t* out, int n, int
         if (base + i < n) out[base + i] = run;
         run += v[i];
     }
+    const int total = s_warp[NW - 1];
     __syncthreads();
+    return total;
 }
 
 // Add each slot's per-warp start to its within-warp rank (s_cnt now holds
 // the exclusive scan over warps). With PLACE (one-block paths) the expert's
 // offset is added too and the result is final: it goes to perm/inv_perm when
-// a.write_out and, if s_inv is given, to s_inv[s] (shared memory).
-template <int GS, int NT, bool PLACE>
+// a.write_out and, if s_inv is given, to s_inv[s] (shared memory). Slots of
+// uncounted experts (LOCAL) get inv_perm -1.
+template <int GS, int NT, bool PLACE, bool LOCAL = false>
 __device__ __forceinline__ void finish_ranks(const RouteArgs& a, int t0, int t1, const int32_t* s_cnt,
                                              const int32_t* s_off, const int (&re)[kRegRounds],
                                              const int (&rr)[kRegRounds], int32_t* s_inv = nullptr) {
@@ -281,13 +293,13 @@ __device__ __forceinline__ void finish_ranks(const RouteArgs& a, int t0, int t1,
     const int warp = threadIdx.x / kWarp;
     const int grp = lane / GS;
     const int gl = lane % GS;
-    const int32_t* start = s_cnt + (size_t)warp * a.E;
+    const int32_t* start = s_cnt + (size_t)warp * a.nloc;
     const int w0 = t0 + warp * a.tpw;
     const int w1 = min(t1, w0 + a.tpw);
 #pragma unroll
     for (int r = 0; r < kRegRounds; ++r) {
+        const int s = (w0 + r * GPW + grp) * a.k + gl;
         if (re[r] >= 0) {
-            const int s = (w0 + r * GPW + grp) * a.k + gl;
             int p = rr[r] + start[re[r]];
             if constexpr (PLACE) {
                 p += s_off[re[r]];
@@ -295,13 +307,20 @@ __device__ __forceinline__ void finish_ranks(const RouteArgs& a, int t0, int t1,
                 if (s_inv != nullptr) s_inv[s] = p;
             }
             if (a.write_out) a.inv_perm[s] = p;
+        } else if (LOCAL && re[r] == -2) {
+            if (a.write_out) a.inv_perm[s] = -1;
+            if (PLACE && s_inv != nullptr) s_inv[s] = -1;
         }
     }
     // slots of rounds past kRegRounds (the two-kernel path only, where
     // write_out holds): the rank was kept in inv_perm
     const int s_lo = (w0 + kRegRounds * GPW) * a.k;
     for (int s = s_lo + lane; s < w1 * a.k; s += kWarp) {
-        const int e = __ldcg(a.topk_ids + s);
+        int e = __ldcg(a.topk_ids + s);
+        if constexpr (LOCAL) {
+            e -= a.e0;
+            if (e < 0 || e >= a.nloc) continue;   // inv_perm already -1
+        }
         int p = __ldcg(a.inv_perm + s) + start[e];
         if constexpr (PLACE) {
             p += s_off[e];

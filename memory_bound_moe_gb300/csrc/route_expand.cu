@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kNt) route_expand_kernel(RouteArgs a, const ui
     constexpr int NW = kNt / kWarp;
     extern __shared__ int32_t smem[];
     int32_t* s_cnt = smem;                      // [NW][E]
-    int32_t* s_tot = s_cnt + (size_t)NW * a.E;  // [Ep] totals, then offsets
+    int32_t* s_tot = s_cnt + (size_t)NW * a.nloc;  // [Ep] totals, then offsets
     int32_t* s_warp = s_tot + a.Ep;             // [32]
     int32_t* s_inv = s_warp + 32;               // [T*k] sorted row of every slot
     pdl_wait_and_release();
@@ -53,12 +53,12 @@ __global__ void __launch_bounds__(kNt) route_expand_kernel(RouteArgs a, const ui
 
     RouteArgs la = a;
     la.write_out = blockIdx.x == 0;
-    for (int i = threadIdx.x; i < NW * a.E; i += kNt) s_cnt[i] = 0;
+    for (int i = threadIdx.x; i < NW * a.nloc; i += kNt) s_cnt[i] = 0;
     __syncthreads();
     int re[kRegRounds], rr[kRegRounds];
     topk_rank_range<GS, EPL, kNt>(la, 0, a.T, s_cnt, re, rr);
     __syncthreads();
-    scan_over_warps<kNt>(s_cnt, s_tot, a.E);
+    scan_over_warps<kNt>(s_cnt, s_tot, a.nloc);
     __syncthreads();
     if (la.write_out)
         for (int e = threadIdx.x; e < a.E; e += kNt) a.expert_counts[e] = s_tot[e];
@@ -133,6 +133,7 @@ cudaError_t launch_route_expand(const RoutePlan& plan, const float* logits, int 
     RouteArgs a;
     a.logits = logits;
     a.T = T; a.E = E; a.k = k; a.renorm = renorm;
+    a.e0 = 0; a.nloc = E; a.pad = 1; a.rows = T * k;
     a.Ep = plan.Ep; a.tpc = plan.tpc; a.tpw = plan.tpw; a.G = 1;
     a.topk_ids = topk_ids; a.topk_weights = topk_weights;
     a.expert_counts = expert_counts; a.expert_offsets = expert_offsets;

@@ -155,6 +155,38 @@ def test_route_expand_rejects_bad_arguments(lib):
     assert call(p=p) == INVALID
 
 
+def test_local_routing_rules(lib):
+    rows = ctypes.c_int64(0)
+    assert lib.moe_route_local_rows(100, 8, 16, 32, 128, ctypes.byref(rows)) == OK
+    assert rows.value == 100 * 8 + 16 * 127
+    assert lib.moe_route_local_rows(100, 8, 32, 32, 1, ctypes.byref(rows)) == INVALID   # empty range
+    assert lib.moe_route_local_rows(100, 8, 0, 4, 0, ctypes.byref(rows)) == INVALID     # pad < 1
+    ws = ctypes.c_size_t(0)
+    assert lib.moe_route_local_workspace_size(4096, 128, 8, 0, 32, ctypes.byref(ws)) == OK
+    full = ctypes.c_size_t(0)
+    assert lib.moe_route_workspace_size(4096, 128, 8, ctypes.byref(full)) == OK
+    assert 0 < ws.value <= full.value            # narrower count matrix
+    assert lib.moe_route_local_workspace_size(4096, 128, 8, 0, 129, ctypes.byref(ws)) == INVALID
+
+    def call(e0=0, e1=32, pad=16, T=16, E=64, k=4, p=None):
+        p = list(A[:7]) if p is None else p
+        return lib.moe_route_local(p[0], T, E, k, 1, e0, e1, pad, p[1], p[2], p[3], p[4], p[5], p[6],
+                                   0, 0, None)
+    assert call(e0=-1) == INVALID
+    assert call(e1=65) == INVALID
+    assert call(e0=10, e1=10) == INVALID
+    assert call(pad=0) == INVALID
+    assert call(T=4096, E=128, k=8) == WORKSPACE
+    p = list(A[:7])
+    p[5] = p[0] + 4                               # perm over the logits
+    assert call(p=p) == INVALID
+    # rows-bounded expand / combine
+    assert lib.moe_expand_rows(A[0], 16, 256, 2, A[1], -1, A[2], None) == INVALID
+    assert lib.moe_expand_rows(A[0], 16, 250, 2, A[1], 40, A[2], None) == MISALIGNED
+    assert lib.moe_combine_rows(A[0], 40, 16, 256, 2, A[1], A[2], A[0] + 512, None) == INVALID
+    assert lib.moe_combine_rows(A[0], -3, 16, 256, 2, A[1], A[2], A[3], None) == INVALID
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import torch
     from memory_bound_moe_gb300 import moe_swiglu
