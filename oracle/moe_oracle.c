@@ -381,3 +381,34 @@ int oracle_combine(const uint16_t* expert_out, long S, int H, int k, long T,
     free(acc);
     return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* QK RMSNorm: per-head RMS normalisation of q and k                       */
+/* ---------------------------------------------------------------------- */
+
+/* "CuTeDSL at Perplexity", section "QK normalization": the QK norm of recent
+ * Qwen attention layers normalises every head of q and of k (64, 128 or 256
+ * elements) with RMS normalisation and a per-head-dimension weight plus a
+ * constant weight bias; its kernel computes rms = rsqrt(sum(x^2)/head_dim +
+ * EPS) and stores ((w + WEIGHT_BIAS) * (x * rms)) in the element type, in
+ * place. (The page's one-line formula omits the reciprocal square root that
+ * its kernel applies; the kernel is followed.)
+ *   y[h, i] = bf16( (w[i] + bias) * x[h, i] / sqrt(mean_i x[h, i]^2 + eps) )
+ * over heads h of x [heads, head_dim] (row-major), real arithmetic, one
+ * rounding. w is bfloat16 [head_dim]. Writes y (may equal x). */
+void oracle_rmsnorm_heads(const uint16_t* x, long heads, int head_dim, const uint16_t* w,
+                          double bias, double eps, uint16_t* y) {
+    for (long h = 0; h < heads; ++h) {
+        const uint16_t* xr = x + h * (long)head_dim;
+        double ss = 0.0;
+        for (int i = 0; i < head_dim; ++i) {
+            double v = bf16_to_double(xr[i]);
+            ss += v * v;
+        }
+        double inv = 1.0 / sqrt(ss / head_dim + eps);
+        for (int i = 0; i < head_dim; ++i) {
+            double v = bf16_to_double(xr[i]);
+            y[h * (long)head_dim + i] = bf16_round((bf16_to_double(w[i]) + bias) * (v * inv));
+        }
+    }
+}

@@ -71,6 +71,9 @@ def _load():
         lib.oracle_quant_mxfp8.argtypes = [_u16p, ctypes.c_long, ctypes.c_int,
                                            ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_uint8)]
         lib.oracle_quant_mxfp8.restype = None
+        lib.oracle_rmsnorm_heads.argtypes = [_u16p, ctypes.c_long, ctypes.c_int, _u16p, ctypes.c_double,
+                                             ctypes.c_double, _u16p]
+        lib.oracle_rmsnorm_heads.restype = None
         lib.oracle_expand.argtypes = [_u16p, ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                       _i32p, ctypes.c_long, _u16p]
         lib.oracle_expand.restype = ctypes.c_int
@@ -280,6 +283,25 @@ def dequant_mxfp8(codes, scales) -> np.ndarray:
     rows, n = codes.shape
     x = np.asarray(scales).astype(np.float64) - 127.0
     return e4m3_decode(codes) * np.repeat(2.0 ** x, 32, axis=1).reshape(rows, n)
+
+
+def rmsnorm_heads(x, w, bias: float, eps: float) -> np.ndarray:
+    """Per-head RMSNorm: x [..., head_dim] bfloat16 bits, w [head_dim];
+    returns bf16((w + bias) * x / sqrt(mean(x^2) + eps))."""
+    x = _c(x, np.uint16)
+    w = _c(w, np.uint16)
+    hd = x.shape[-1]
+    assert w.shape == (hd,)
+    out = np.empty_like(x)
+    _load().oracle_rmsnorm_heads(_ptr(x, ctypes.c_uint16), x.size // hd, hd, _ptr(w, ctypes.c_uint16),
+                                 float(bias), float(eps), _ptr(out, ctypes.c_uint16))
+    return out
+
+
+def qk_norm(q, k, q_weight, k_weight, bias: float, eps: float):
+    """QK norm of q [T, nq, hd] and k [T, nk, hd]: each head normalised with
+    its tensor's weight. Returns (q_out, k_out)."""
+    return rmsnorm_heads(q, q_weight, bias, eps), rmsnorm_heads(k, k_weight, bias, eps)
 
 
 def path(logits, x, gate_up, expert_out, k: int, renorm: bool):

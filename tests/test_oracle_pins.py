@@ -545,3 +545,48 @@ def test_mxfp8_round_trip_error_bound(oracle_mod):
     assert np.all(np.abs(deq - xv)[inside] <= bound[inside])
     assert np.all(np.abs(deq[~inside]) == 448 * 2.0 ** X[~inside])
     assert np.all(np.sign(deq) * np.sign(xv) >= 0)
+
+
+# ---------------------------------------------------------------------------
+# QK RMSNorm
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("hd", [64, 128, 256])
+def test_rmsnorm_matches_torch_rms_norm(oracle_mod, hd):
+    O = oracle_mod
+    rng = np.random.default_rng(hd)
+    x = O.bf16_round(rng.standard_normal((200, hd)) * np.exp(rng.uniform(-3, 3, (200, 1))))
+    w = O.bf16_round(rng.standard_normal(hd) * 0.1)
+    bias, eps = 1.0, 1e-6
+    xt = torch.from_numpy(O.bf16_decode(x))
+    wt = torch.from_numpy(O.bf16_decode(w)) + bias
+    ref = torch.nn.functional.rms_norm(xt, (hd,), wt, eps).numpy()
+    assert np.array_equal(O.rmsnorm_heads(x, w, bias, eps), O.bf16_round(ref))
+
+
+def test_rmsnorm_closed_forms(oracle_mod):
+    O = oracle_mod
+    hd = 128
+    one = O.bf16_round(np.ones(hd))
+    zero_w = O.bf16_round(np.zeros(hd))
+    # a constant head c with eps = 0: x / rms(x) = sign(c); with w = 0, bias 1
+    for c in (3.0, -0.25, 1e-20):
+        x = O.bf16_round(np.full((1, hd), c))
+        assert np.all(O.bf16_decode(O.rmsnorm_heads(x, zero_w, 1.0, 0.0)) == np.sign(c))
+    # the weight multiplies, the bias adds to it: w = 1, bias = 0.5 -> 1.5 * sign
+    x = O.bf16_round(np.full((1, hd), -7.0))
+    assert np.all(O.bf16_decode(O.rmsnorm_heads(x, one, 0.5, 0.0)) == -1.5)
+    # a head of +-1 alternating with eps = 3: 1 / sqrt(1 + 3) = 0.5
+    x = O.bf16_round(np.tile([1.0, -1.0], hd // 2)[None, :])
+    assert np.all(O.bf16_decode(O.rmsnorm_heads(x, zero_w, 1.0, 3.0)) == np.tile([0.5, -0.5], hd // 2))
+    # scale invariance (eps = 0, power-of-two scale: exact)
+    rng = np.random.default_rng(4)
+    x = O.bf16_round(rng.standard_normal((50, hd)))
+    x8 = O.bf16_round(O.bf16_decode(x) * 8.0)
+    w = O.bf16_round(rng.standard_normal(hd))
+    assert np.array_equal(O.rmsnorm_heads(x, w, 0.0, 0.0), O.rmsnorm_heads(x8, w, 0.0, 0.0))
+    # every head is normalised on its own: one head's values do not leak
+    xx = x.copy()
+    xx[7] = O.bf16_round(rng.standard_normal(hd) * 1000)
+    a, b = O.rmsnorm_heads(x, w, 0.0, 1e-6), O.rmsnorm_heads(xx, w, 0.0, 1e-6)
+    assert np.array_equal(np.delete(a, 7, 0), np.delete(b, 7, 0))
