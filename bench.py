@@ -470,6 +470,88 @@ def decode_latency(dev, reps=2000):
     return {kk: (round(v, 3) if isinstance(v, float) else v) for kk, v in res.items()}
 
 
+def extras_measurement(dev, reps=200):
+    """The wider entry points on the mid workload (T=4096, H=2048, E=128,
+    top-8, I=768), each launched back to back over two input sets (so every
+    launch reads its inputs from HBM): MXFP8 SwiGLU and expand against their
+    bfloat16 versions, and one tensor-parallel rank's local routing (experts
+    [0, 32) of 128, segments padded to 128 rows) with its padded expand and
+    partial combine. GB/s = algorithmic bytes / time."""
+    import torch
+    import memory_bound_moe_gb300 as moe
+    from memory_bound_moe_gb300.workloads import WORKLOADS, generate
+    lib = moe.load_library()
+    w = WORKLOADS["mid"]
+    T, H, E, k, I, S = w.T, w.H, w.E, w.k, w.I, w.S
+    peak, _ = peak_hbm()
+    sets = []
+    for seed in (0, 1):
+        inp = {kk: v.to(dev) for kk, v in generate(w, seed=seed).items()}
+        inp["r"] = moe.moe_route(inp["logits"], k, True)
+        sets.append(inp)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    p = lambda t: t.data_ptr()
+    i32 = dict(dtype=torch.int32, device=dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    outs = {
+        "act": torch.empty((S, I), dtype=torch.bfloat16, device=dev),
+        "act_c": torch.empty((S, I), **u8), "act_s": torch.empty((S, I // 32), **u8),
+        "ex": torch.empty((S, H), dtype=torch.bfloat16, device=dev),
+        "ex_c": torch.empty((S, H), **u8), "ex_s": torch.empty((S, H // 32), **u8),
+    }
+    e0, e1, pad = 0, 32, 128
+    rows = moe.moe_route_local_rows(T, k, e0, e1, pad)
+    loc = [moe.moe_route_local(d["logits"], k, True, e0, e1, pad) for d in sets]
+    ws = torch.empty((max(moe.moe_route_local_workspace_size(T, E, k, e0, e1), 16),), **u8)
+    lex = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+    leo = [torch.randn((rows, H), device=dev).to(torch.bfloat16) for _ in sets]
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+
+    def timed(fns):
+        for f in fns:
+            f()
+        torch.cuda.synchronize(dev)
+        torch.cuda._sleep(4_000_000)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for r in range(reps):
+            assert fns[r % len(fns)]() == 0
+        b.record()
+        torch.cuda.synchronize(dev)
+        return 1e3 * a.elapsed_time(b) / reps
+
+    n_loc = int(sum(int(l.expert_counts.sum()) for l in loc) / len(loc))   # local slots per batch
+    cases = {
+        "swiglu_bf16": ([lambda d=d: lib.moe_swiglu(p(d["gate_up"]), S, I, p(outs["act"]), sp) for d in sets],
+                        6 * S * I),
+        "swiglu_mxfp8": ([lambda d=d: lib.moe_swiglu_mxfp8(p(d["gate_up"]), S, I, p(outs["act_c"]),
+                                                           p(outs["act_s"]), sp) for d in sets],
+                         4 * S * I + S * I + S * I // 32),
+        "expand_bf16": ([lambda d=d: lib.moe_expand(p(d["x"]), T, H, k, p(d["r"].inv_perm), p(outs["ex"]), sp)
+                         for d in sets], 2 * T * H + 2 * S * H + 4 * S),
+        "expand_mxfp8": ([lambda d=d: lib.moe_expand_mxfp8(p(d["x"]), T, H, k, p(d["r"].inv_perm), S,
+                                                           p(outs["ex_c"]), p(outs["ex_s"]), sp) for d in sets],
+                         2 * T * H + S * H + S * H // 32 + 4 * S),
+        "route_local_rank0of4": ([lambda d=d, l=l: lib.moe_route_local(
+            p(d["logits"]), T, E, k, 1, e0, e1, pad, p(l.topk_ids), p(l.topk_weights), p(l.expert_counts),
+            p(l.expert_offsets), p(l.perm), p(l.inv_perm), p(ws), ws.numel(), sp)
+            for d, l in zip(sets, loc)], 4 * T * E + 12 * S + 4 * rows),
+        "expand_rows_rank0of4": ([lambda d=d, l=l: lib.moe_expand_rows(p(d["x"]), T, H, k, p(l.inv_perm), rows,
+                                                                         p(lex), sp) for d, l in zip(sets, loc)],
+                                 2 * T * H + 2 * n_loc * H + 4 * S),
+        "combine_rows_rank0of4": ([lambda e=e, l=l: lib.moe_combine_rows(p(e), rows, T, H, k, p(l.topk_weights),
+                                                                           p(l.inv_perm), p(out), sp)
+                                   for e, l in zip(leo, loc)], 2 * n_loc * H + 8 * S + 2 * T * H),
+    }
+    res = {"workload": w.describe(), "local_rank": f"experts [{e0},{e1}) of {E}, pad {pad}, {n_loc} local slots"}
+    for name, (fns, nbytes) in cases.items():
+        us = timed(fns)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[name] = {"us": round(us, 3), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    return res
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
@@ -657,6 +739,7 @@ def main():
                       "out copied back on a separate stream"}
 
     decode = decode_latency(dev) if args.workload == WORKLOAD else None
+    extras = extras_measurement(dev) if args.workload == WORKLOAD else None
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
@@ -670,6 +753,7 @@ def main():
             "roofline": roofline, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": step.launches_per_step * args.steps,
             "decode_latency": decode,
+            "extras": extras,
             "clocks": clk, "remeasured": remeasured, "wall_s_timed_region": round(wall, 3),
             "device": torch.cuda.get_device_name(dev),
         }

@@ -293,6 +293,51 @@ moe_status_t moe_combine_rows(const moe_bf16_t* expert_out, int64_t rows, int64_
                               const float* topk_weights, const int32_t* inv_perm,
                               moe_bf16_t* out, moe_stream_t stream);
 
+/*
+ * MXFP8 outputs for the next expert GEMM.
+ * "CuTeDSL at Perplexity", section "Blackwell support": Blackwell supports
+ * MXFP8 / MXFP4 / NVFP4 in hardware and the kernels were adapted for FP8
+ * block-wise scaling, with absolute maxima over 32-element (MX) blocks.
+ * Block format (OCP Microscaling v1.0, MXFP8 E4M3): for every 32 consecutive
+ * values of a row with largest magnitude amax,
+ *   X = floor(log2 amax) - 8, clamped to [-127, 127] (-127 if amax = 0)
+ *   scale byte (E8M0) = X + 127;  code = E4M3(v * 2^-X), round to nearest
+ *   even, saturated to +-448.  Dequantized value: E4M3(code) * 2^X.
+ * codes [rows, n] bytes (16-byte aligned), scales [rows, n/32] bytes, both
+ * row-major; n (I or H) must be a multiple of 32 (MOE_ERR_MISALIGNED).
+ * The values quantized are the bfloat16 values moe_swiglu / moe_expand would
+ * store. Inputs are assumed finite.
+ *
+ * moe_swiglu_mxfp8: act = silu(gate) * up as moe_swiglu, then quantized.
+ * moe_expand_mxfp8: token rows quantized once and written to the k rows
+ *   inv_perm[t*k + j] < rows of the code and scale buffers (rows as for
+ *   moe_expand_rows: T*k, or a padded local capacity).
+ */
+moe_status_t moe_swiglu_mxfp8(const moe_bf16_t* gate_up, int64_t rows, int I,
+                              uint8_t* act_codes, uint8_t* act_scales, moe_stream_t stream);
+moe_status_t moe_expand_mxfp8(const moe_bf16_t* x, int64_t T, int H, int k,
+                              const int32_t* inv_perm, int64_t rows,
+                              uint8_t* codes, uint8_t* scales, moe_stream_t stream);
+
+/*
+ * QK RMSNorm, in place, for the attention layer of the same models.
+ * "CuTeDSL at Perplexity", section "QK normalization": recent Qwen models
+ * normalise every head of q and of k (64, 128 or 256 elements) with RMS
+ * normalisation, a per-dimension weight and a constant weight bias; the
+ * page's kernel stores ((w + bias) * (x * rsqrt(sum(x^2)/head_dim + eps))).
+ *
+ *   q[t, h, :] = bf16_rn( (q_weight + weight_bias) * q[t, h, :] * r ),
+ *   r = 1 / sqrt(mean(q[t, h, :]^2) + eps)   (float32), likewise k with k_weight.
+ * q [T, num_q_heads, head_dim], k [T, num_k_heads, head_dim] (bfloat16,
+ * row-major, 16-byte aligned; either head count may be 0 and its pointer
+ * then NULL), q_weight / k_weight [head_dim]. head_dim must be 64, 128 or 256
+ * (MOE_ERR_UNSUPPORTED). q and k must not overlap the weights.
+ */
+moe_status_t moe_qk_rmsnorm(moe_bf16_t* q, moe_bf16_t* k, int64_t T, int num_q_heads,
+                            int num_k_heads, int head_dim, const moe_bf16_t* q_weight,
+                            const moe_bf16_t* k_weight, float weight_bias, float eps,
+                            moe_stream_t stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

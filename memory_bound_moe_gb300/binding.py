@@ -72,6 +72,13 @@ def load_library():
         lib.moe_expand_rows.restype = _int
         lib.moe_combine_rows.argtypes = [_vp, _i64, _i64, _int, _int, _vp, _vp, _vp, _vp]
         lib.moe_combine_rows.restype = _int
+        lib.moe_swiglu_mxfp8.argtypes = [_vp, _i64, _int, _vp, _vp, _vp]
+        lib.moe_swiglu_mxfp8.restype = _int
+        lib.moe_expand_mxfp8.argtypes = [_vp, _i64, _int, _int, _vp, _i64, _vp, _vp, _vp]
+        lib.moe_expand_mxfp8.restype = _int
+        lib.moe_qk_rmsnorm.argtypes = [_vp, _vp, _i64, _int, _int, _int, _vp, _vp, ctypes.c_float,
+                                       ctypes.c_float, _vp]
+        lib.moe_qk_rmsnorm.restype = _int
         lib.moe_expand.argtypes = [_vp, _i64, _int, _int, _vp, _vp, _vp]
         lib.moe_expand.restype = _int
         lib.moe_swiglu.argtypes = [_vp, _i64, _int, _vp, _vp]
@@ -362,3 +369,71 @@ def moe_combine_rows(expert_out: torch.Tensor, topk_weights: torch.Tensor, inv_p
                                                                _ptr(topk_weights), _ptr(inv_perm), _ptr(out),
                                                                _stream_ptr(stream, expert_out.device)))
     return out
+
+
+# ---------------------------------------------------------------------------
+# MXFP8 outputs (E4M3 codes, E8M0 scale per 32 values)
+# ---------------------------------------------------------------------------
+
+def moe_swiglu_mxfp8(gate_up: torch.Tensor, *, codes: Optional[torch.Tensor] = None,
+                     scales: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None):
+    """SwiGLU of ``gate_up [rows, 2I]`` quantized to MXFP8: returns
+    ``(codes uint8 [rows, I], scales uint8 [rows, I/32])``."""
+    rows, two_i = gate_up.shape
+    I = two_i // 2
+    _need(gate_up, "gate_up", torch.bfloat16, (rows, two_i))
+    dev = gate_up.device
+    if codes is None:
+        codes = torch.empty((rows, I), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty((rows, I // 32), dtype=torch.uint8, device=dev)
+    _need(codes, "act_codes", torch.uint8, (rows, I))
+    _need(scales, "act_scales", torch.uint8, (rows, I // 32))
+    _check("moe_swiglu_mxfp8", load_library().moe_swiglu_mxfp8(_ptr(gate_up), rows, I, _ptr(codes),
+                                                               _ptr(scales), _stream_ptr(stream, dev)))
+    return codes, scales
+
+
+def moe_expand_mxfp8(x: torch.Tensor, inv_perm: torch.Tensor, k: int, rows: Optional[int] = None, *,
+                     codes: Optional[torch.Tensor] = None, scales: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None):
+    """Expansion of ``x [T, H]`` quantized to MXFP8 into ``rows`` rows
+    (default T*k): returns ``(codes uint8 [rows, H], scales uint8 [rows, H/32])``."""
+    T, H = x.shape
+    _need(x, "x", torch.bfloat16, (T, H))
+    _need(inv_perm, "inv_perm", torch.int32, (T * k,))
+    rows = T * k if rows is None else rows
+    dev = x.device
+    if codes is None:
+        codes = torch.empty((rows, H), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty((rows, H // 32), dtype=torch.uint8, device=dev)
+    _need(codes, "codes", torch.uint8, (rows, H))
+    _need(scales, "scales", torch.uint8, (rows, H // 32))
+    _check("moe_expand_mxfp8", load_library().moe_expand_mxfp8(_ptr(x), T, H, int(k), _ptr(inv_perm), rows,
+                                                               _ptr(codes), _ptr(scales),
+                                                               _stream_ptr(stream, dev)))
+    return codes, scales
+
+
+# ---------------------------------------------------------------------------
+# QK RMSNorm (in place)
+# ---------------------------------------------------------------------------
+
+def moe_qk_rmsnorm(q: torch.Tensor, k: torch.Tensor, q_weight: torch.Tensor, k_weight: torch.Tensor,
+                   weight_bias: float = 0.0, eps: float = 1e-6, *,
+                   stream: Optional[torch.cuda.Stream] = None):
+    """Per-head RMSNorm of ``q [T, nq, head_dim]`` and ``k [T, nk, head_dim]``
+    (bfloat16) in place: ``(w + weight_bias) * x * rsqrt(mean(x^2) + eps)``.
+    Returns ``(q, k)``."""
+    T, nq, hd = q.shape
+    nk = k.shape[1]
+    _need(q, "q", torch.bfloat16, (T, nq, hd))
+    _need(k, "k", torch.bfloat16, (T, nk, hd))
+    _need(q_weight, "q_weight", torch.bfloat16, (hd,))
+    _need(k_weight, "k_weight", torch.bfloat16, (hd,))
+    _check("moe_qk_rmsnorm", load_library().moe_qk_rmsnorm(_ptr(q), _ptr(k), T, nq, nk, hd, _ptr(q_weight),
+                                                           _ptr(k_weight), float(weight_bias), float(eps),
+                                                           _stream_ptr(stream, q.device)))
+    return q, k

@@ -373,4 +373,71 @@ moe_status_t moe_combine(const moe_bf16_t* expert_out, int64_t T, int H, int k,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_swiglu_mxfp8(const moe_bf16_t* gate_up, int64_t rows, int I, uint8_t* act_codes,
+                              uint8_t* act_scales, moe_stream_t stream) {
+    moe_status_t st = check_rows(rows, I, 1);
+    if (st != MOE_OK) return st;
+    if (I % 32 != 0) return MOE_ERR_MISALIGNED;
+    if (rows == 0) return MOE_OK;
+    if (gate_up == nullptr || act_codes == nullptr || act_scales == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(gate_up) || !aligned16(act_codes)) return MOE_ERR_MISALIGNED;
+    const uint64_t n = uint64_t(rows) * uint64_t(I);
+    if (any_overlap({{act_codes, n}, {act_scales, n / 32}}, {{gate_up, 4 * n}}))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_swiglu_mxfp8(gate_up, rows, I, act_codes, act_scales, sms,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_expand_mxfp8(const moe_bf16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
+                              int64_t rows, uint8_t* codes, uint8_t* scales, moe_stream_t stream) {
+    if (k < 1) return MOE_ERR_INVALID_ARG;
+    if (k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
+    moe_status_t st = check_rows(T, H, k);
+    if (st != MOE_OK) return st;
+    if (H % 32 != 0) return MOE_ERR_MISALIGNED;
+    if (rows < 0) return MOE_ERR_INVALID_ARG;
+    if (rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (T == 0 || rows == 0) return MOE_OK;
+    if (x == nullptr || inv_perm == nullptr || codes == nullptr || scales == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned4(inv_perm)) return MOE_ERR_MISALIGNED;
+    const uint64_t S = uint64_t(T) * uint64_t(k);
+    const uint64_t n = uint64_t(rows) * uint64_t(H);
+    if (any_overlap({{codes, n}, {scales, n / 32}},
+                    {{x, 2 * uint64_t(T) * uint64_t(H)}, {inv_perm, 4 * S}}))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_expand_mxfp8(x, T, H, k, inv_perm, rows, codes, scales, sms,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_qk_rmsnorm(moe_bf16_t* q, moe_bf16_t* k, int64_t T, int num_q_heads,
+                            int num_k_heads, int head_dim, const moe_bf16_t* q_weight,
+                            const moe_bf16_t* k_weight, float weight_bias, float eps,
+                            moe_stream_t stream) {
+    if (T < 0 || num_q_heads < 0 || num_k_heads < 0 || num_q_heads + num_k_heads < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return MOE_ERR_UNSUPPORTED;
+    if (T * int64_t(num_q_heads + num_k_heads) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if ((num_q_heads > 0 && q == nullptr) || (num_k_heads > 0 && k == nullptr) ||
+        q_weight == nullptr || k_weight == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if ((num_q_heads > 0 && !aligned16(q)) || (num_k_heads > 0 && !aligned16(k)) ||
+        !aligned16(q_weight) || !aligned16(k_weight))
+        return MOE_ERR_MISALIGNED;
+    const uint64_t qb = 2 * uint64_t(T) * uint64_t(num_q_heads) * uint64_t(head_dim);
+    const uint64_t kb = 2 * uint64_t(T) * uint64_t(num_k_heads) * uint64_t(head_dim);
+    if (any_overlap({{q, qb}, {k, kb}}, {{q_weight, 2ull * head_dim}, {k_weight, 2ull * head_dim}}))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_qk_rmsnorm(q, k, T, num_q_heads, num_k_heads, head_dim, q_weight,
+                                            k_weight, weight_bias, eps, sms,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -60,4 +60,18 @@ cudaError_t launch_combine(const uint16_t* expert_out, int64_t rows, int64_t T, 
                            const float* topk_weights, const int32_t* inv_perm, uint16_t* out,
                            int num_sms, cudaStream_t stream);
 
+// SwiGLU / expand with MXFP8 outputs (quant.cu): codes [rows, n] E4M3 bytes,
+// scales [rows, n/32] E8M0 bytes; n (I or H) a multiple of 32.
+cudaError_t launch_swiglu_mxfp8(const uint16_t* gate_up, int64_t rows, int I, uint8_t* codes,
+                                uint8_t* scales, int num_sms, cudaStream_t stream);
+cudaError_t launch_expand_mxfp8(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
+                                int64_t rows, uint8_t* codes, uint8_t* scales, int num_sms,
+                                cudaStream_t stream);
+
+// Per-head RMSNorm of q [T, nq, head_dim] and k [T, nk, head_dim] in place
+// (qknorm.cu); head_dim 64, 128 or 256.
+cudaError_t launch_qk_rmsnorm(uint16_t* q, uint16_t* k, int64_t T, int nq, int nk, int head_dim,
+                              const uint16_t* qw, const uint16_t* kw, float bias, float eps,
+                              int num_sms, cudaStream_t stream);
+
 }  // namespace moe

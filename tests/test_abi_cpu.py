@@ -25,6 +25,17 @@ def lib():
     return binding.load_library()
 
 
+@pytest.fixture(scope="module")
+def nogpu():
+    # The validation tests pass fake device addresses that are never
+    # dereferenced because every call fails validation first; on a machine
+    # with a GPU they are skipped anyway, so no slip in a test can ever launch
+    # a kernel on such an address.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("fake-address validation tests run only on hosts without a GPU")
+
+
 def _declared_functions():
     names = []
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
@@ -81,7 +92,7 @@ def _route(lib, T=64, E=8, k=2, ptrs=None, ws=0, ws_bytes=0):
     return lib.moe_route(p[0], T, E, k, 1, p[1], p[2], p[3], p[4], p[5], p[6], ws, ws_bytes, None)
 
 
-def test_route_rejects_bad_arguments(lib):
+def test_route_rejects_bad_arguments(lib, nogpu):
     assert _route(lib, k=9) == INVALID
     assert _route(lib, k=0) == INVALID
     assert _route(lib, T=-3) == INVALID
@@ -108,7 +119,7 @@ def test_route_rejects_bad_arguments(lib):
     assert _route(lib, ptrs=p) == INVALID
 
 
-def test_expand_swiglu_combine_reject_bad_arguments(lib):
+def test_expand_swiglu_combine_reject_bad_arguments(lib, nogpu):
     # expand(x, T, H, k, inv_perm, out, stream)
     assert lib.moe_expand(A[0], 16, 256, 0, A[1], A[2], None) == INVALID
     assert lib.moe_expand(A[0], 16, 256, 17, A[1], A[2], None) == UNSUPPORTED
@@ -136,7 +147,7 @@ def test_expand_swiglu_combine_reject_bad_arguments(lib):
     assert lib.moe_combine(0, 0, 256, 2, 0, 0, 0, None) == OK
 
 
-def test_route_expand_rejects_bad_arguments(lib):
+def test_route_expand_rejects_bad_arguments(lib, nogpu):
     def call(T=16, E=64, k=4, H=256, x=A[7], ex=A[8], ws=0, ws_bytes=0, p=None):
         p = list(A[:7]) if p is None else p
         return lib.moe_route_expand(p[0], T, E, k, 1, x, H, p[1], p[2], p[3], p[4], p[5], p[6],
@@ -155,7 +166,7 @@ def test_route_expand_rejects_bad_arguments(lib):
     assert call(p=p) == INVALID
 
 
-def test_local_routing_rules(lib):
+def test_local_routing_rules(lib, nogpu):
     rows = ctypes.c_int64(0)
     assert lib.moe_route_local_rows(100, 8, 16, 32, 128, ctypes.byref(rows)) == OK
     assert rows.value == 100 * 8 + 16 * 127
@@ -185,6 +196,31 @@ def test_local_routing_rules(lib):
     assert lib.moe_expand_rows(A[0], 16, 250, 2, A[1], 40, A[2], None) == MISALIGNED
     assert lib.moe_combine_rows(A[0], 40, 16, 256, 2, A[1], A[2], A[0] + 512, None) == INVALID
     assert lib.moe_combine_rows(A[0], -3, 16, 256, 2, A[1], A[2], A[3], None) == INVALID
+
+
+def test_mxfp8_rules(lib, nogpu):
+    assert lib.moe_swiglu_mxfp8(A[0], 16, 48, A[1], A[2], None) == MISALIGNED     # I % 32
+    assert lib.moe_swiglu_mxfp8(A[0], 16, 64, A[1] + 8, A[2], None) == MISALIGNED  # codes alignment
+    assert lib.moe_swiglu_mxfp8(A[0], 16, 64, 0, A[2], None) == INVALID
+    assert lib.moe_swiglu_mxfp8(A[0], 16, 64, A[0] + 64, A[2], None) == INVALID   # codes over gate_up
+    assert lib.moe_swiglu_mxfp8(0, 0, 64, 0, 0, None) == OK
+    assert lib.moe_expand_mxfp8(A[0], 16, 264, 2, A[1], 32, A[2], A[3], None) == MISALIGNED  # H % 32
+    assert lib.moe_expand_mxfp8(A[0], 16, 256, 2, A[1], -1, A[2], A[3], None) == INVALID
+    assert lib.moe_expand_mxfp8(A[0], 16, 256, 2, A[1], 32, A[2], 0, None) == INVALID
+    assert lib.moe_expand_mxfp8(A[0], 16, 256, 2, A[1], 32, A[0], A[3], None) == INVALID   # codes over x
+
+
+def test_qk_rmsnorm_rules(lib, nogpu):
+    f = lambda *a: lib.moe_qk_rmsnorm(*a)
+    import ctypes as C
+    lib.moe_qk_rmsnorm.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_int, C.c_int, C.c_int,
+                                   C.c_void_p, C.c_void_p, C.c_float, C.c_float, C.c_void_p]
+    assert f(A[0], A[1], 16, 32, 4, 96, A[2], A[3], 0.0, 1e-6, None) == UNSUPPORTED   # head_dim
+    assert f(A[0], A[1], 16, 0, 0, 128, A[2], A[3], 0.0, 1e-6, None) == INVALID
+    assert f(A[0] + 8, A[1], 16, 32, 4, 128, A[2], A[3], 0.0, 1e-6, None) == MISALIGNED
+    assert f(A[0], A[1], 16, 32, 4, 128, A[2] + 2, A[3], 0.0, 1e-6, None) == MISALIGNED
+    assert f(A[0], A[1], 16, 32, 4, 128, A[0] + 256, A[3], 0.0, 1e-6, None) == INVALID  # weight in q
+    assert f(0, 0, 0, 32, 4, 128, A[2], A[3], 0.0, 1e-6, None) == OK
 
 
 def test_binding_refuses_cpu_tensors(lib):
