@@ -39,6 +39,15 @@ __device__ __forceinline__ void ld_stream(Bits<32>& v, const void* p) {
                  : "l"(p));
 }
 
+// Coherent 128-bit load (no L1 allocation) for data the same kernel writes
+// back in place, where the non-coherent path's read-only contract would not
+// hold.
+__device__ __forceinline__ void ld_coherent(Bits<16>& v, const void* p) {
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+}
+
 __device__ __forceinline__ void st_global(void* p, const Bits<16>& v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])

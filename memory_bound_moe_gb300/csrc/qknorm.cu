@@ -1,0 +1,147 @@
+// QK RMSNorm: per-head RMS normalisation of q and k, in place.
+//
+// "CuTeDSL at Perplexity", section "QK normalization": the QK norm of recent
+// Qwen attention layers is applied per head of 64, 128 or 256 elements. Unlike
+// a general RMSNorm over thousands of elements it needs no cross-warp
+// reduction: with 128 bits (8 bfloat16) per thread a half warp covers a
+// 128-element head, the squared norm is a butterfly shuffle over those lanes,
+// and several heads share a warp; the weight bias and epsilon are
+// compile-time constants there (runtime arguments here), the result is
+// ((w + bias) * (x * rsqrt(sum(x^2)/head_dim + eps))) stored in place.
+//
+// Here: head h of the flattened [T, nq + nk] list of heads is handled by
+// HD/8 lanes (one 16-byte vector each); q heads use q_weight, k heads
+// k_weight. Each thread loads its q and k weight chunks (plus the bias) once,
+// since a thread always covers the same 8 columns, then sweeps heads
+// grid-stride, U head groups per iteration with all loads issued first.
+#include "moe_device.cuh"
+#include "moe_launch.h"
+#include "rows_common.cuh"
+
+namespace moe {
+namespace {
+
+template <int HD, int U, int NT>
+__global__ void __launch_bounds__(NT) qk_norm_kernel(uint8_t* __restrict__ q, uint8_t* __restrict__ k,
+                                                     int nq, int nk, uint32_t heads, DivU32 per_token,
+                                                     const uint8_t* __restrict__ qw,
+                                                     const uint8_t* __restrict__ kw, float bias,
+                                                     float eps) {
+    constexpr int TPH = HD / 8;        // lanes per head
+    constexpr int HPW = kWarp / TPH;   // heads per warp
+    pdl_wait_and_release();
+    const int lane = threadIdx.x % kWarp;
+    const int sub = lane % TPH;        // this thread's 8 columns: sub*8 .. sub*8 + 7
+    float wq[8], wk[8];
+    {
+        Bits<16> a, b;
+        ld_stream(a, qw + sub * 16);
+        ld_stream(b, kw + sub * 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            wq[2 * i] = bf16_lo(a.w[i]) + bias;
+            wq[2 * i + 1] = bf16_hi(a.w[i]) + bias;
+            wk[2 * i] = bf16_lo(b.w[i]) + bias;
+            wk[2 * i + 1] = bf16_hi(b.w[i]) + bias;
+        }
+    }
+    const uint32_t warps = gridDim.x * (NT / kWarp);
+    const uint32_t gwarp = blockIdx.x * (NT / kWarp) + threadIdx.x / kWarp;
+    const uint32_t stride = warps * HPW * U;
+    // warp-uniform loop: lanes whose head is past the end compute on zeros
+    for (uint32_t base = gwarp * HPW * U; base < heads; base += stride) {
+        Bits<16> x[U];
+        uint8_t* ptr[U];
+        bool isq[U];
+        bool valid[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t h = base + u * HPW + lane / TPH;
+            valid[u] = h < heads;
+            ptr[u] = nullptr;
+            isq[u] = true;
+            if (valid[u]) {
+                const uint32_t t = per_token.div(h);
+                const int j = int(h - t * per_token.d);
+                isq[u] = j < nq;
+                ptr[u] = isq[u] ? q + (uint64_t(t) * nq + j) * (2 * HD) + sub * 16
+                                : k + (uint64_t(t) * nk + (j - nq)) * (2 * HD) + sub * 16;
+                ld_coherent(x[u], ptr[u]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) x[u].w[i] = 0u;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float v[8];
+            float ss = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = bf16_lo(x[u].w[i]);
+                v[2 * i + 1] = bf16_hi(x[u].w[i]);
+                ss = fmaf(v[2 * i], v[2 * i], ss);
+                ss = fmaf(v[2 * i + 1], v[2 * i + 1], ss);
+            }
+#pragma unroll
+            for (int o = TPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+            const float rms = rsqrtf(ss / float(HD) + eps);
+            if (valid[u]) {
+                Bits<16> y;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float w0 = isq[u] ? wq[2 * i] : wk[2 * i];
+                    const float w1 = isq[u] ? wq[2 * i + 1] : wk[2 * i + 1];
+                    y.w[i] = pack_bf16x2(w0 * (v[2 * i] * rms), w1 * (v[2 * i + 1] * rms));
+                }
+                st_global(ptr[u], y);
+            }
+        }
+    }
+}
+
+#ifndef MOE_QKNORM_NT
+#define MOE_QKNORM_NT 256
+#endif
+#ifndef MOE_QKNORM_UNROLL
+#define MOE_QKNORM_UNROLL 2
+#endif
+constexpr int kNt = MOE_QKNORM_NT;
+constexpr int kU = MOE_QKNORM_UNROLL;
+
+template <int HD>
+cudaError_t launch_hd(uint16_t* q, uint16_t* k, int64_t T, int nq, int nk, const uint16_t* qw,
+                      const uint16_t* kw, float bias, float eps, int num_sms, cudaStream_t stream) {
+    auto kernel = qk_norm_kernel<HD, kU, kNt>;
+    static const int occ = resident_blocks(kernel, kNt);
+    constexpr int HPW = kWarp / (HD / 8);
+    const int per = nq + nk;
+    const int64_t tok_per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / per));
+    for (int64_t t0 = 0; t0 < T; t0 += tok_per_launch) {
+        const int64_t nt = std::min(tok_per_launch, T - t0);
+        const uint32_t heads = uint32_t(nt * per);
+        const uint64_t per_block = uint64_t(kNt / kWarp) * HPW * kU;
+        const int grid = grid_for(occ, heads, per_block, num_sms);
+        const cudaError_t err = launch_pdl(
+            kernel, dim3(grid), dim3(kNt), 0, stream, reinterpret_cast<uint8_t*>(q + t0 * nq * int64_t(HD)),
+            reinterpret_cast<uint8_t*>(k + t0 * nk * int64_t(HD)), nq, nk, heads, DivU32::make(uint32_t(per)),
+            reinterpret_cast<const uint8_t*>(qw), reinterpret_cast<const uint8_t*>(kw), bias, eps);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_qk_rmsnorm(uint16_t* q, uint16_t* k, int64_t T, int nq, int nk, int head_dim,
+                              const uint16_t* qw, const uint16_t* kw, float bias, float eps,
+                              int num_sms, cudaStream_t stream) {
+    switch (head_dim) {
+        case 64: return launch_hd<64>(q, k, T, nq, nk, qw, kw, bias, eps, num_sms, stream);
+        case 128: return launch_hd<128>(q, k, T, nq, nk, qw, kw, bias, eps, num_sms, stream);
+        case 256: return launch_hd<256>(q, k, T, nq, nk, qw, kw, bias, eps, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace moe
