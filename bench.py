@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle CPU work for the cpu_baseline leg (0 = skip)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the decode-latency and wider-entry-point measurements")
     return ap.parse_args()
 
 
@@ -470,13 +472,16 @@ def decode_latency(dev, reps=2000):
     return {kk: (round(v, 3) if isinstance(v, float) else v) for kk, v in res.items()}
 
 
-def extras_measurement(dev, reps=200):
+def extras_measurement(dev, reps=240, n_sets=3):
     """The wider entry points on the mid workload (T=4096, H=2048, E=128,
-    top-8, I=768), each launched back to back over two input sets (so every
-    launch reads its inputs from HBM): MXFP8 SwiGLU and expand against their
-    bfloat16 versions, and one tensor-parallel rank's local routing (experts
-    [0, 32) of 128, segments padded to 128 rows) with its padded expand and
-    partial combine. GB/s = algorithmic bytes / time."""
+    top-8, I=768), each launched back to back over three sets of inputs AND
+    outputs (each set larger than half of L2, so every launch reads from and
+    writes back to HBM): MXFP8 SwiGLU and expand against their bfloat16
+    versions; one tensor-parallel rank's local routing (experts [0, 32) of
+    128, segments padded to 128 rows) with its padded expand and partial
+    combine; and the QK RMSNorm of a Qwen3-30B-A3B-like attention layer
+    (T=8192, 32 q heads, 4 k heads, head_dim 128, in place). GB/s =
+    algorithmic bytes / time."""
     import torch
     import memory_bound_moe_gb300 as moe
     from memory_bound_moe_gb300.workloads import WORKLOADS, generate
@@ -484,32 +489,34 @@ def extras_measurement(dev, reps=200):
     w = WORKLOADS["mid"]
     T, H, E, k, I, S = w.T, w.H, w.E, w.k, w.I, w.S
     peak, _ = peak_hbm()
-    sets = []
-    for seed in (0, 1):
-        inp = {kk: v.to(dev) for kk, v in generate(w, seed=seed).items()}
-        inp["r"] = moe.moe_route(inp["logits"], k, True)
-        sets.append(inp)
     sp = torch.cuda.current_stream(dev).cuda_stream
     p = lambda t: t.data_ptr()
-    i32 = dict(dtype=torch.int32, device=dev)
     u8 = dict(dtype=torch.uint8, device=dev)
-    outs = {
-        "act": torch.empty((S, I), dtype=torch.bfloat16, device=dev),
-        "act_c": torch.empty((S, I), **u8), "act_s": torch.empty((S, I // 32), **u8),
-        "ex": torch.empty((S, H), dtype=torch.bfloat16, device=dev),
-        "ex_c": torch.empty((S, H), **u8), "ex_s": torch.empty((S, H // 32), **u8),
-    }
+    bf = dict(dtype=torch.bfloat16, device=dev)
     e0, e1, pad = 0, 32, 128
     rows = moe.moe_route_local_rows(T, k, e0, e1, pad)
-    loc = [moe.moe_route_local(d["logits"], k, True, e0, e1, pad) for d in sets]
     ws = torch.empty((max(moe.moe_route_local_workspace_size(T, E, k, e0, e1), 16),), **u8)
-    lex = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
-    leo = [torch.randn((rows, H), device=dev).to(torch.bfloat16) for _ in sets]
-    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    sets = []
+    for seed in range(n_sets):
+        d = {kk: v.to(dev) for kk, v in generate(w, seed=seed).items()}
+        d["r"] = moe.moe_route(d["logits"], k, True)
+        d["act"] = torch.empty((S, I), **bf)
+        d["act_c"], d["act_s"] = torch.empty((S, I), **u8), torch.empty((S, I // 32), **u8)
+        d["ex"] = torch.empty((S, H), **bf)
+        d["ex_c"], d["ex_s"] = torch.empty((S, H), **u8), torch.empty((S, H // 32), **u8)
+        d["loc"] = moe.moe_route_local(d["logits"], k, True, e0, e1, pad)
+        d["lex"] = torch.empty((rows, H), **bf)
+        d["leo"] = torch.randn((rows, H), device=dev).to(torch.bfloat16)
+        d["out"] = torch.empty((T, H), **bf)
+        sets.append(d)
+    qT, nq, nk, hd = 8192, 32, 4, 128
+    qk = [(torch.randn((qT, nq, hd), device=dev).to(torch.bfloat16),
+           torch.randn((qT, nk, hd), device=dev).to(torch.bfloat16)) for _ in range(n_sets)]
+    qkw = (torch.randn(hd, device=dev).to(torch.bfloat16), torch.randn(hd, device=dev).to(torch.bfloat16))
 
     def timed(fns):
         for f in fns:
-            f()
+            assert f() == 0
         torch.cuda.synchronize(dev)
         torch.cuda._sleep(4_000_000)
         a = torch.cuda.Event(enable_timing=True)
@@ -521,30 +528,36 @@ def extras_measurement(dev, reps=200):
         torch.cuda.synchronize(dev)
         return 1e3 * a.elapsed_time(b) / reps
 
-    n_loc = int(sum(int(l.expert_counts.sum()) for l in loc) / len(loc))   # local slots per batch
+    n_loc = int(sum(int(d["loc"].expert_counts.sum()) for d in sets) / n_sets)   # local slots per batch
     cases = {
-        "swiglu_bf16": ([lambda d=d: lib.moe_swiglu(p(d["gate_up"]), S, I, p(outs["act"]), sp) for d in sets],
+        "swiglu_bf16": ([lambda d=d: lib.moe_swiglu(p(d["gate_up"]), S, I, p(d["act"]), sp) for d in sets],
                         6 * S * I),
-        "swiglu_mxfp8": ([lambda d=d: lib.moe_swiglu_mxfp8(p(d["gate_up"]), S, I, p(outs["act_c"]),
-                                                           p(outs["act_s"]), sp) for d in sets],
+        "swiglu_mxfp8": ([lambda d=d: lib.moe_swiglu_mxfp8(p(d["gate_up"]), S, I, p(d["act_c"]), p(d["act_s"]),
+                                                           sp) for d in sets],
                          4 * S * I + S * I + S * I // 32),
-        "expand_bf16": ([lambda d=d: lib.moe_expand(p(d["x"]), T, H, k, p(d["r"].inv_perm), p(outs["ex"]), sp)
+        "expand_bf16": ([lambda d=d: lib.moe_expand(p(d["x"]), T, H, k, p(d["r"].inv_perm), p(d["ex"]), sp)
                          for d in sets], 2 * T * H + 2 * S * H + 4 * S),
         "expand_mxfp8": ([lambda d=d: lib.moe_expand_mxfp8(p(d["x"]), T, H, k, p(d["r"].inv_perm), S,
-                                                           p(outs["ex_c"]), p(outs["ex_s"]), sp) for d in sets],
+                                                           p(d["ex_c"]), p(d["ex_s"]), sp) for d in sets],
                          2 * T * H + S * H + S * H // 32 + 4 * S),
-        "route_local_rank0of4": ([lambda d=d, l=l: lib.moe_route_local(
-            p(d["logits"]), T, E, k, 1, e0, e1, pad, p(l.topk_ids), p(l.topk_weights), p(l.expert_counts),
-            p(l.expert_offsets), p(l.perm), p(l.inv_perm), p(ws), ws.numel(), sp)
-            for d, l in zip(sets, loc)], 4 * T * E + 12 * S + 4 * rows),
-        "expand_rows_rank0of4": ([lambda d=d, l=l: lib.moe_expand_rows(p(d["x"]), T, H, k, p(l.inv_perm), rows,
-                                                                         p(lex), sp) for d, l in zip(sets, loc)],
+        "route_local_rank0of4": ([lambda d=d: lib.moe_route_local(
+            p(d["logits"]), T, E, k, 1, e0, e1, pad, p(d["loc"].topk_ids), p(d["loc"].topk_weights),
+            p(d["loc"].expert_counts), p(d["loc"].expert_offsets), p(d["loc"].perm), p(d["loc"].inv_perm),
+            p(ws), ws.numel(), sp) for d in sets], 4 * T * E + 12 * S + 4 * rows),
+        "expand_rows_rank0of4": ([lambda d=d: lib.moe_expand_rows(p(d["x"]), T, H, k, p(d["loc"].inv_perm), rows,
+                                                                    p(d["lex"]), sp) for d in sets],
                                  2 * T * H + 2 * n_loc * H + 4 * S),
-        "combine_rows_rank0of4": ([lambda e=e, l=l: lib.moe_combine_rows(p(e), rows, T, H, k, p(l.topk_weights),
-                                                                           p(l.inv_perm), p(out), sp)
-                                   for e, l in zip(leo, loc)], 2 * n_loc * H + 8 * S + 2 * T * H),
+        "combine_rows_rank0of4": ([lambda d=d: lib.moe_combine_rows(p(d["leo"]), rows, T, H, k,
+                                                                      p(d["loc"].topk_weights), p(d["loc"].inv_perm),
+                                                                      p(d["out"]), sp) for d in sets],
+                                  2 * n_loc * H + 8 * S + 2 * T * H),
+        "qk_rmsnorm_qwen3": ([lambda q=q, kk=kk: lib.moe_qk_rmsnorm(p(q), p(kk), qT, nq, nk, hd, p(qkw[0]),
+                                                                       p(qkw[1]), 1.0, 1e-6, sp)
+                              for q, kk in qk], 2 * 2 * qT * (nq + nk) * hd),
     }
-    res = {"workload": w.describe(), "local_rank": f"experts [{e0},{e1}) of {E}, pad {pad}, {n_loc} local slots"}
+    res = {"workload": w.describe(), "local_rank": f"experts [{e0},{e1}) of {E}, pad {pad}, {n_loc} local slots",
+           "qk_rmsnorm": f"T={qT} q_heads={nq} k_heads={nk} head_dim={hd}, in place",
+           "timing": f"{reps} back-to-back launches over {n_sets} sets of inputs and outputs"}
     for name, (fns, nbytes) in cases.items():
         us = timed(fns)
         gbs = nbytes / (us * 1e-6) / 1e9
@@ -738,8 +751,9 @@ def main():
                       "double-buffered device sets; the C-ABI calls through the Python binding; "
                       "out copied back on a separate stream"}
 
-    decode = decode_latency(dev) if args.workload == WORKLOAD else None
-    extras = extras_measurement(dev) if args.workload == WORKLOAD else None
+    more = args.workload == WORKLOAD and not args.no_extras
+    decode = decode_latency(dev) if more else None
+    extras = extras_measurement(dev) if more else None
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:

@@ -57,7 +57,7 @@ def test_qk_rmsnorm_zero_heads_and_eps(dev, oracle_mod):
     hd = 128
     q = np.zeros((4, 2, hd), dtype=np.uint16)            # all-zero heads: 0 * rsqrt(eps) = 0
     q[1, 1] = O.bf16_round(np.full(hd, 2.0))
-    k = O.bf16_round(np.tile([1.0, -1.0], hd // 2)[None, None, :].repeat(3, 0))
+    k = O.bf16_round(np.tile([1.0, -1.0], hd // 2)[None, None, :].repeat(4, 0))
     w = O.bf16_round(np.zeros(hd))
     qd, kd = bf16_dev(q, dev), bf16_dev(k, dev)
     moe_qk_rmsnorm(qd, kd, bf16_dev(w, dev), bf16_dev(w, dev), 1.0, 3.0)
