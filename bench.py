@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the decode-latency and wider-entry-point measurements")
+    ap.add_argument("--extra-reps", type=int, default=0,
+                    help="repetitions per case in those measurements (0: 2000 decode, 240 others)")
     return ap.parse_args()
 
 
@@ -752,8 +754,8 @@ def main():
                       "out copied back on a separate stream"}
 
     more = args.workload == WORKLOAD and not args.no_extras
-    decode = decode_latency(dev) if more else None
-    extras = extras_measurement(dev) if more else None
+    decode = decode_latency(dev, reps=args.extra_reps or 2000) if more else None
+    extras = extras_measurement(dev, reps=args.extra_reps or 240) if more else None
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:

@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(NT) route_place_kernel(RouteArgs a) {
     __syncthreads();
     for (int c = threadIdx.x; c < Ep; c += NT) {
         int tot = 0, pre = 0;
+#pragma unroll 8
         for (int r = 0; r < R; ++r) { tot += s_ptot[r * Ep + c]; pre += s_ppre[r * Ep + c]; }
         s_tot[c] = tot;
         s_base[c] = pre;

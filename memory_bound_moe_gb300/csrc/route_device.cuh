@@ -223,12 +223,14 @@ template <int NT>
 __device__ __forceinline__ void scan_over_warps(int32_t* s_cnt, int32_t* s_tot, int E) {
     constexpr int NW = NT / kWarp;
     for (int e = threadIdx.x; e < E; e += NT) {
+        int v[NW];   // all loads first: one shared-memory round trip, not NW
+#pragma unroll
+        for (int w = 0; w < NW; ++w) v[w] = s_cnt[(size_t)w * E + e];
         int run = 0;
-#pragma unroll 4
+#pragma unroll
         for (int w = 0; w < NW; ++w) {
-            const int v = s_cnt[(size_t)w * E + e];
             s_cnt[(size_t)w * E + e] = run;
-            run += v;
+            run += v[w];
         }
         s_tot[e] = run;
     }
