@@ -89,7 +89,7 @@ def peak_hbm():
 
 
 KERNEL_SOURCES = {
-    "route": ["route.cu"],
+    "route": ["route.cu", "route_device.cuh", "rows_common.cuh"],
     "expand": ["expand.cu", "rows_common.cuh"],
     "swiglu": ["swiglu.cu", "rows_common.cuh"],
     "combine": ["combine.cu", "rows_common.cuh"],
