@@ -295,6 +295,7 @@ cudaError_t launch_route(const RoutePlan& plan, const float* logits, int T, int 
     a.perm = perm; a.inv_perm = inv_perm;
     a.ws_counts = static_cast<int32_t*>(workspace);
     a.write_out = true;
+    a.vec4 = E % 4 == 0 && reinterpret_cast<uintptr_t>(logits) % 16 == 0;
     return local ? launch_route_local<true>(plan, a, stream) : launch_route_local<false>(plan, a, stream);
 }
 

@@ -28,7 +28,11 @@ struct RouteArgs {
     int32_t* inv_perm;
     int32_t* ws_counts;  // [G][Ep]
     bool write_out;      // write topk_ids/weights, perm, inv_perm (false: block-private results)
+    bool vec4;           // logits rows may be read as 16-byte vectors (E % 4 == 0, 16-byte base)
 };
+
+// Largest k the selection loop unrolls for (the public MOE_MAX_TOPK).
+constexpr int kMaxTopk = 16;
 
 // Order-preserving map of a float onto uint32 (larger float -> larger key).
 // -0.0 is first folded onto +0.0 so that the two compare equal. Key 0 marks
@@ -76,71 +80,138 @@ __device__ __forceinline__ float group_sum(float v) {
     return v;
 }
 
-// Keys of token t for lane gl of a GS-lane group: experts gl, gl + GS, ...
-// (a coalesced row read) as order-preserving keys; 0 outside the row.
+// Keys of token t for lane gl of a GS-lane group: the EPL consecutive experts
+// gl*EPL .. gl*EPL + EPL - 1, so that lane order is expert order, as
+// order-preserving keys; 0 outside the row. Whole 16-byte vectors when the
+// row layout allows it.
 template <int GS, int EPL>
 __device__ __forceinline__ void load_keys(const RouteArgs& a, int t, bool valid, int gl,
                                           uint32_t (&key)[EPL]) {
-    const float* row = a.logits + (size_t)t * a.E;
+    const int e0 = gl * EPL;
+    const float* row = a.logits + (size_t)t * a.E + e0;
+    if constexpr (EPL % 4 == 0) {
+        if (a.vec4 && valid && e0 + EPL <= a.E) {
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        const int e = gl + GS * i;
-        key[i] = (valid && e < a.E) ? order_key(__ldg(row + e)) : 0u;
+            for (int q = 0; q < EPL / 4; ++q) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(row) + q);
+                key[4 * q] = order_key(v.x);
+                key[4 * q + 1] = order_key(v.y);
+                key[4 * q + 2] = order_key(v.z);
+                key[4 * q + 3] = order_key(v.w);
+            }
+            return;
+        }
     }
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+        key[i] = (valid && e0 + i < a.E) ? order_key(__ldg(row + i)) : 0u;
 }
 
-// Top-k of one token by a group of GS lanes from its keys (the float is
-// recovered exactly from its key). Each of the k rounds takes the group
-// maximum of the keys and, among lanes holding it, the lowest expert index;
-// the owner then drops that expert. Lane j < k keeps the j-th pick, writes it
-// and its weight, and returns the expert (-1 for lanes without a pick). Every
-// lane of the warp must call (valid may differ between groups of one warp;
-// invalid groups compute on empty keys and write nothing).
+// Top-k of one token by a group of GS lanes holding its keys in expert order
+// (the float is recovered exactly from its key). Pick j is the largest key
+// left and, among equal keys, the lowest expert. Each lane offers its best key
+// (the lowest of its experts among equal keys); the pick is the group maximum
+// of the offers, taken from the lowest lane offering it, which holds the
+// lowest such expert since lanes hold consecutive experts. One group maximum
+// and one ballot per pick.
+//   EPL <= 8: a lane first sorts its keys in descending order by swapping
+//   neighbours only when the later key is strictly larger, so equal keys keep
+//   their expert order; its offer is then the head of the list, and the
+//   owner of a pick shifts its list by one. The expert of every sorted
+//   position is packed into one register, LB bits each.
+//   EPL > 8: a lane takes the arg-max of its keys every round and the owner
+//   zeroes the picked key.
+// Lane j < k keeps the j-th pick, writes it and its weight, and returns the
+// expert (-1 for lanes without a pick). Every lane of the warp must call
+// (valid may differ between groups of one warp; invalid groups compute on
+// empty keys and write nothing).
 template <int GS, int EPL>
 __device__ __forceinline__ int topk_select(const RouteArgs& a, int t, bool valid, int gl,
                                            uint32_t (&key)[EPL]) {
+    constexpr bool kSorted = EPL <= 8;
+    constexpr int LB = EPL <= 2 ? 1 : EPL <= 4 ? 2 : 3;
+    constexpr uint32_t kIdxMask = (1u << LB) - 1u;
+    const int lane = threadIdx.x % kWarp;
+    const unsigned gmask = GS == 32 ? kFull : (((1u << GS) - 1u) << (lane & ~(GS - 1)));
+
+    uint32_t pidx = 0;   // sorted: expert index (within the lane) of position q at bits q*LB
+    if constexpr (kSorted) {
+        uint32_t ix[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) ix[i] = uint32_t(i);
+#pragma unroll
+        for (int p = 0; p < EPL; ++p) {
+#pragma unroll
+            for (int i = p & 1; i + 1 < EPL; i += 2) {
+                const bool sw = key[i + 1] > key[i];
+                const uint32_t k0 = sw ? key[i + 1] : key[i], k1 = sw ? key[i] : key[i + 1];
+                const uint32_t i0 = sw ? ix[i + 1] : ix[i], i1 = sw ? ix[i] : ix[i + 1];
+                key[i] = k0; key[i + 1] = k1; ix[i] = i0; ix[i + 1] = i1;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) pidx |= ix[i] << (i * LB);
+    }
+    // this lane's offer: best key and its expert index within the lane
+    auto offer = [&](uint32_t& bk, int& bi) {
+        if constexpr (kSorted) {
+            bk = key[0];
+            bi = int(pidx & kIdxMask);
+        } else {
+            bk = key[0];
+            bi = 0;
+#pragma unroll
+            for (int i = 1; i < EPL; ++i)
+                if (key[i] > bk) { bk = key[i]; bi = i; }
+        }
+    };
+
+    uint32_t bk;
+    int bi;
+    offer(bk, bi);
+    const uint32_t top = group_max<GS>(bk);   // the first pick's key
+    const float vmax = key_value(top);
     // Softmax denominator over all E experts (only without renormalisation),
     // taken before the picks remove keys.
     float z = 0.0f;
     if (!a.renorm) {
-        uint32_t lmax = key[0];
-#pragma unroll
-        for (int i = 1; i < EPL; ++i) lmax = max(lmax, key[i]);
-        const float vmax = key_value(group_max<GS>(lmax));
 #pragma unroll
         for (int i = 0; i < EPL; ++i)
             if (key[i] != 0u) z += expf(key_value(key[i]) - vmax);
         z = group_sum<GS>(z);
     }
 
+    uint32_t my_key = 0;
     int my_id = 0;
-    float my_val = 0.0f;
-    float vmax = 0.0f;
-    for (int j = 0; j < a.k; ++j) {
-        uint32_t bk = key[0];
-        int bi = 0;
 #pragma unroll
-        for (int i = 1; i < EPL; ++i) {
-            if (key[i] > bk) { bk = key[i]; bi = i; }
-        }
-        const uint32_t gk = group_max<GS>(bk);
-        const uint32_t cand = (bk == gk) ? uint32_t(gl + GS * bi) : 0xffffffffu;
-        const uint32_t ge = group_min<GS>(cand);
-        if (int(ge % GS) == gl) {
-            const int wi = int(ge / GS);
+    for (int j = 0; j < kMaxTopk; ++j) {
+        if (j >= a.k) break;
+        if (j > 0) offer(bk, bi);
+        const uint32_t gk = (j == 0) ? top : group_max<GS>(bk);
+        const unsigned bal = __ballot_sync(kFull, bk == gk) & gmask;
+        const int ol = __ffs(bal) - 1;   // owner: a lane of this group
+        const int id = __shfl_sync(kFull, gl * EPL + bi, ol);
+        const bool own = ol == lane;
+        if constexpr (kSorted) {
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) if (i == wi) key[i] = 0u;
+            for (int i = 0; i + 1 < EPL; ++i) key[i] = own ? key[i + 1] : key[i];
+            key[EPL - 1] = own ? 0u : key[EPL - 1];
+            pidx = own ? pidx >> LB : pidx;
+        } else {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) key[i] = (own && i == bi) ? 0u : key[i];
         }
-        const float gv = key_value(gk);
-        if (j == 0) vmax = gv;
-        if (gl == j) { my_id = int(ge); my_val = gv; }
+        if (gl == j) { my_key = gk; my_id = id; }
     }
 
     // Weights in float32. The largest logit is the first pick.
     const bool mine = gl < a.k;
-    const float ej = mine ? expf(my_val - vmax) : 0.0f;
-    const float denom = a.renorm ? group_sum<GS>(ej)   // sum over the k picks
-                                 : z;                  // sum over all E experts
+    const float ej = mine ? expf(key_value(my_key) - vmax) : 0.0f;
+    float denom = z;                       // sum over all E experts
+    if (a.renorm) {                        // sum over the k picks (lanes 0..k-1)
+        denom = ej;
+        for (int o = 1; o < a.k; o <<= 1) denom += __shfl_xor_sync(kFull, denom, o);
+    }
     if (valid && mine) {
         if (a.write_out) {
             a.topk_ids[(size_t)t * a.k + gl] = my_id;

@@ -140,6 +140,7 @@ cudaError_t launch_route_expand(const RoutePlan& plan, const float* logits, int 
     a.perm = perm; a.inv_perm = inv_perm;
     a.ws_counts = nullptr;
     a.write_out = true;
+    a.vec4 = E % 4 == 0 && reinterpret_cast<uintptr_t>(logits) % 16 == 0;
     switch (plan.gs * 100 + plan.epl) {
         case 801: return launch_gs<8, 1>(a, x, H, expanded_x, num_sms, stream);
         case 1601: return launch_gs<16, 1>(a, x, H, expanded_x, num_sms, stream);
