@@ -61,10 +61,25 @@ __global__ void __launch_bounds__(NT) route_rank_kernel(RouteArgs a) {
     finish_ranks<GS, NT, false, LOCAL>(a, t0, t1, s_cnt, nullptr, re, rr);
 }
 
-// Number of row groups the place kernel splits the count matrix into.
-__host__ __device__ inline int place_rowgroups(int Ep, int nt) {
-    const int cg = Ep / 4;
-    return cg >= nt ? 1 : nt / cg;
+// The place kernel's split of the count matrix: column groups of 4 experts
+// (int4), padded to a power of two below a warp so that the lanes of a warp
+// sharing a column group are a shuffle butterfly apart; row groups (one per
+// thread and column group); and the partial rows left after the in-warp sum.
+struct PlaceSplit {
+    int CG, CGp, R, LPW, Rp;
+};
+__host__ __device__ inline PlaceSplit place_split(int Ep, int nt) {
+    PlaceSplit q;
+    q.CG = Ep / 4;
+    q.CGp = q.CG;
+    if (q.CG < kWarp) {
+        q.CGp = 1;
+        while (q.CGp < q.CG) q.CGp <<= 1;
+    }
+    q.R = q.CGp >= nt ? 1 : nt / q.CGp;
+    q.LPW = q.CGp < kWarp ? kWarp / q.CGp : 1;
+    q.Rp = q.R / q.LPW;
+    return q;
 }
 
 // Offsets from the block's expert totals s_tot[0..nloc): the exclusive scan
@@ -89,6 +104,45 @@ __device__ __forceinline__ int compute_offsets(const RouteArgs& a, const int32_t
     return total;
 }
 
+// Offsets by one warp (lane l scans a contiguous run of experts) from the
+// expert totals s_tot[0..nloc): the exclusive scan of the counts, each rounded
+// up to a multiple of pad for a local routing. Writes s_off[0..nloc]
+// (s_off[nloc] = total rows used), adds the offsets to s_base and, when `out`,
+// writes expert_counts and expert_offsets.
+template <bool LOCAL>
+__device__ __forceinline__ void warp_offsets(const RouteArgs& a, const int32_t* s_tot, int32_t* s_off,
+                                             int32_t* s_base, bool out) {
+    const int lane = threadIdx.x % kWarp;
+    const int per = (a.nloc + kWarp - 1) / kWarp;
+    const int e0 = lane * per;
+    const int e1 = min(a.nloc, e0 + per);
+    auto rows_of = [&](int c) { return LOCAL ? (c + a.pad - 1) / a.pad * a.pad : c; };
+    int local = 0;
+    for (int e = e0; e < e1; ++e) local += rows_of(s_tot[e]);
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    const int total = __shfl_sync(kFull, x, kWarp - 1);
+    int run = x - local;
+    for (int e = e0; e < e1; ++e) {
+        const int c = s_tot[e];
+        s_off[e] = run;
+        s_base[e] += run;
+        if (out) {
+            a.expert_counts[e] = c;
+            a.expert_offsets[e] = run;
+        }
+        run += rows_of(c);
+    }
+    if (lane == 0) {
+        s_off[a.nloc] = total;
+        if (out) a.expert_offsets[a.nloc] = total;
+    }
+}
+
 // perm = -1 on the padding rows of local experts l = l0, l0 + dl, ... and on
 // the rows [total + r0, rows) in steps of dr (block-strided by the caller).
 template <int NT>
@@ -103,67 +157,86 @@ template <int NT, bool LOCAL>
 __global__ void __launch_bounds__(NT) route_place_kernel(RouteArgs a) {
     extern __shared__ int32_t smem[];
     const int Ep = a.Ep;
-    const int CG = Ep / 4;
-    const int R = place_rowgroups(Ep, NT);
-    int32_t* s_ptot = smem;                 // [R][Ep]
-    int32_t* s_ppre = s_ptot + R * Ep;      // [R][Ep]
-    int32_t* s_tot = s_ppre + R * Ep;       // [Ep]
+    const PlaceSplit q = place_split(Ep, NT);
+    int32_t* s_ptot = smem;                 // [Rp][Ep]
+    int32_t* s_ppre = s_ptot + q.Rp * Ep;   // [Rp][Ep]
+    int32_t* s_tot = s_ppre + q.Rp * Ep;    // [Ep]
     int32_t* s_base = s_tot + Ep;           // [Ep]
     int32_t* s_off = s_base + Ep;           // [Ep + 4]
-    int32_t* s_warp = s_off + Ep + 4;       // [32]
     const int b = blockIdx.x;
     pdl_wait_and_release();
 
+    // This thread's first slot, read before the count matrix so that both
+    // loads are in flight together.
+    const int s0 = b * a.tpc * a.k;
+    const int s1 = min(a.T, (b + 1) * a.tpc) * a.k;
+    const int sf = s0 + threadIdx.x;
+    int ef = 0, rf = 0;
+    if (sf < s1) {
+        ef = __ldcg(a.topk_ids + sf);
+        rf = __ldcg(a.inv_perm + sf);
+    }
+
     // Column sums of the count matrix over all blocks (totals) and over the
-    // blocks before this one (prefix). Rows are interleaved over R row
-    // groups; columns are read as int4, contiguous across a warp.
-    for (int idx = threadIdx.x; idx < R * CG; idx += NT) {
-        const int r = idx / CG;
-        const int cg = idx % CG;
+    // blocks before this one (prefix). Thread (r, cg) sums rows r, r + R, ...
+    // of column group cg, read as int4 (contiguous across the lanes of one
+    // row); lanes of a warp holding the same column group then add up by
+    // shuffles, leaving Rp partial rows.
+    const int4* mat = reinterpret_cast<const int4*>(a.ws_counts);
+    for (int idx = threadIdx.x; idx < q.R * q.CGp; idx += NT) {
+        const int r = idx / q.CGp;
+        const int cg = idx % q.CGp;
         int4 tot = make_int4(0, 0, 0, 0), pre = make_int4(0, 0, 0, 0);
-        const int4* col = reinterpret_cast<const int4*>(a.ws_counts) + cg;
-        const int q = Ep / 4;   // int4 per row
-        for (int rb0 = r; rb0 < a.G; rb0 += 8 * R) {
-            int4 v[8];
+        if (cg < q.CG) {
+            for (int rb0 = r; rb0 < a.G; rb0 += 8 * q.R) {
+                int4 v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {   // 8 independent loads in flight
-                const int rb = rb0 + u * R;
-                v[u] = rb < a.G ? __ldcg(col + (size_t)rb * q) : make_int4(0, 0, 0, 0);
-            }
+                for (int u = 0; u < 8; ++u) {   // 8 independent loads in flight
+                    const int rb = rb0 + u * q.R;
+                    v[u] = rb < a.G ? __ldcg(mat + (size_t)rb * q.CG + cg) : make_int4(0, 0, 0, 0);
+                }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                tot.x += v[u].x; tot.y += v[u].y; tot.z += v[u].z; tot.w += v[u].w;
-                if (rb0 + u * R < b) { pre.x += v[u].x; pre.y += v[u].y; pre.z += v[u].z; pre.w += v[u].w; }
+                for (int u = 0; u < 8; ++u) {
+                    tot.x += v[u].x; tot.y += v[u].y; tot.z += v[u].z; tot.w += v[u].w;
+                    if (rb0 + u * q.R < b) { pre.x += v[u].x; pre.y += v[u].y; pre.z += v[u].z; pre.w += v[u].w; }
+                }
             }
         }
-        reinterpret_cast<int4*>(s_ptot + r * Ep)[cg] = tot;
-        reinterpret_cast<int4*>(s_ppre + r * Ep)[cg] = pre;
+        // q.LPW > 1 only when q.R * q.CGp == NT: every lane is here
+        for (int o = q.CGp; o < kWarp; o <<= 1) {
+            tot.x += __shfl_xor_sync(kFull, tot.x, o); tot.y += __shfl_xor_sync(kFull, tot.y, o);
+            tot.z += __shfl_xor_sync(kFull, tot.z, o); tot.w += __shfl_xor_sync(kFull, tot.w, o);
+            pre.x += __shfl_xor_sync(kFull, pre.x, o); pre.y += __shfl_xor_sync(kFull, pre.y, o);
+            pre.z += __shfl_xor_sync(kFull, pre.z, o); pre.w += __shfl_xor_sync(kFull, pre.w, o);
+        }
+        if (r % q.LPW == 0 && cg < q.CG) {
+            reinterpret_cast<int4*>(s_ptot + (r / q.LPW) * Ep)[cg] = tot;
+            reinterpret_cast<int4*>(s_ppre + (r / q.LPW) * Ep)[cg] = pre;
+        }
     }
     __syncthreads();
     for (int c = threadIdx.x; c < Ep; c += NT) {
         int tot = 0, pre = 0;
 #pragma unroll 8
-        for (int r = 0; r < R; ++r) { tot += s_ptot[r * Ep + c]; pre += s_ppre[r * Ep + c]; }
+        for (int r = 0; r < q.Rp; ++r) { tot += s_ptot[r * Ep + c]; pre += s_ppre[r * Ep + c]; }
         s_tot[c] = tot;
         s_base[c] = pre;
     }
     __syncthreads();
-    compute_offsets<NT, LOCAL>(a, s_tot, s_off, s_warp, b == 0);
-    for (int e = threadIdx.x; e < a.nloc; e += NT) s_base[e] += s_off[e];
+    if (threadIdx.x < kWarp) warp_offsets<LOCAL>(a, s_tot, s_off, s_base, b == 0);
     __syncthreads();
 
-    const int s0 = b * a.tpc * a.k;
-    const int s1 = min(a.T, (b + 1) * a.tpc) * a.k;
-    for (int s = s0 + threadIdx.x; s < s1; s += NT) {
-        int e = __ldcg(a.topk_ids + s);
+    auto place = [&](int s, int e, int rank) {
         if constexpr (LOCAL) {
             e -= a.e0;
-            if (e < 0 || e >= a.nloc) continue;   // inv_perm already -1
+            if (e < 0 || e >= a.nloc) return;   // inv_perm already -1
         }
-        const int p = s_base[e] + __ldcg(a.inv_perm + s);
+        const int p = s_base[e] + rank;
         a.perm[p] = s;
         a.inv_perm[s] = p;
-    }
+    };
+    if (sf < s1) place(sf, ef, rf);
+    for (int s = sf + NT; s < s1; s += NT) place(s, __ldcg(a.topk_ids + s), __ldcg(a.inv_perm + s));
     if constexpr (LOCAL) fill_padding<NT>(a, s_tot, s_off, b, a.G, b * NT, a.G * NT);
 }
 
@@ -272,8 +345,8 @@ RoutePlan plan_route(int64_t T, int E, int k, int nloc) {
     p.G = int((T + tpc - 1) / tpc);
     p.ws_bytes = sizeof(int32_t) * size_t(p.G) * size_t(p.Ep);
     p.smem_topk = sizeof(int32_t) * (size_t(nw) * nloc + p.Ep);
-    const int R = place_rowgroups(p.Ep, kNtSplit);
-    p.smem_scatter = sizeof(int32_t) * (size_t(2) * R * p.Ep + 3 * size_t(p.Ep) + 4 + 32);
+    const PlaceSplit q = place_split(p.Ep, kNtSplit);
+    p.smem_scatter = sizeof(int32_t) * (size_t(2) * q.Rp * p.Ep + 3 * size_t(p.Ep) + 4);
     return p;
 }
 
