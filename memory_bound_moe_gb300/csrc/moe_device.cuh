@@ -94,6 +94,17 @@ __device__ __forceinline__ void pdl_wait_and_release() {
 }
 
 // --------------------------------------------------------------------------
+// Bulk prefetch of [p, p + bytes) into L2 (no registers, no completion to
+// wait for; p 16-byte aligned, bytes a multiple of 16). Reading data early
+// this way is safe whoever writes it: L2 is the point of coherence, so a
+// later write simply updates the prefetched lines.
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
+// --------------------------------------------------------------------------
 // Unsigned 32-bit division by a divisor fixed for the whole launch, as a
 // multiply-high, an add and a shift (Granlund & Montgomery, "Division by
 // Invariant Integers using Multiplication", PLDI 1994, the round-up variant

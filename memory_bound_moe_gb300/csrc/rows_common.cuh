@@ -62,6 +62,18 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// L2 size of the current device (queried once per process).
+inline uint64_t l2_bytes() {
+    static const uint64_t bytes = [] {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+            return uint64_t(0);
+        return uint64_t(v);
+    }();
+    return bytes;
+}
+
 // Work items per launch stay below 2^31 so 32-bit grid-stride indices never
 // wrap; larger jobs are split into several launches over row ranges.
 constexpr uint64_t kMaxItemsPerLaunch = uint64_t(1) << 30;
