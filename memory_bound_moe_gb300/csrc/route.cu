@@ -46,15 +46,14 @@ __global__ void __launch_bounds__(NT) route_rank_kernel(RouteArgs a) {
     int32_t* s_cnt = smem;                         // [NW][nloc]
     int32_t* s_tot = s_cnt + (size_t)NW * a.nloc;  // [Ep]
     pdl_wait_and_release();
-    for (int i = threadIdx.x; i < NW * a.nloc; i += NT) s_cnt[i] = 0;
-    for (int e = threadIdx.x; e < a.Ep; e += NT) s_tot[e] = 0;
-    __syncthreads();
+    zero_warp_counters(s_cnt, a.nloc);
     const int t0 = blockIdx.x * a.tpc;
     const int t1 = min(a.T, t0 + a.tpc);
     int re[kRegRounds], rr[kRegRounds];
     topk_rank_range<GS, EPL, NT, LOCAL>(a, t0, t1, s_cnt, re, rr);
     __syncthreads();
     scan_over_warps<NT>(s_cnt, s_tot, a.nloc);
+    for (int e = a.nloc + threadIdx.x; e < a.Ep; e += NT) s_tot[e] = 0;
     __syncthreads();
     int32_t* row = a.ws_counts + (size_t)blockIdx.x * a.Ep;
     for (int e = threadIdx.x; e < a.Ep; e += NT) row[e] = s_tot[e];
@@ -249,8 +248,7 @@ __global__ void __launch_bounds__(NT) route_fused_kernel(RouteArgs a) {
     int32_t* s_off = s_tot + a.Ep;                 // [Ep + 4] offsets
     int32_t* s_warp = s_off + a.Ep + 4;            // [32]
     pdl_wait_and_release();
-    for (int i = threadIdx.x; i < NW * a.nloc; i += NT) s_cnt[i] = 0;
-    __syncthreads();
+    zero_warp_counters(s_cnt, a.nloc);
     int re[kRegRounds], rr[kRegRounds];
     topk_rank_range<GS, EPL, NT, LOCAL>(a, 0, a.T, s_cnt, re, rr);
     __syncthreads();

@@ -288,6 +288,15 @@ __device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int 
     }
 }
 
+// Zero this warp's row of the per-warp counters s_cnt[NW][nloc]; only the
+// warp itself touches the row until the scan over warps, so a warp barrier is
+// enough.
+__device__ __forceinline__ void zero_warp_counters(int32_t* s_cnt, int nloc) {
+    int32_t* c = s_cnt + (size_t)(threadIdx.x / kWarp) * nloc;
+    for (int i = threadIdx.x % kWarp; i < nloc; i += kWarp) c[i] = 0;
+    __syncwarp();
+}
+
 // Exclusive scan over warps of s_cnt[w][e] for every expert; s_tot[e] gets
 // the block total.
 template <int NT>

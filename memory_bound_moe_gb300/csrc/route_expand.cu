@@ -53,8 +53,7 @@ __global__ void __launch_bounds__(kNt) route_expand_kernel(RouteArgs a, const ui
 
     RouteArgs la = a;
     la.write_out = blockIdx.x == 0;
-    for (int i = threadIdx.x; i < NW * a.nloc; i += kNt) s_cnt[i] = 0;
-    __syncthreads();
+    zero_warp_counters(s_cnt, a.nloc);
     int re[kRegRounds], rr[kRegRounds];
     topk_rank_range<GS, EPL, kNt>(la, 0, a.T, s_cnt, re, rr);
     __syncthreads();
