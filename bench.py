@@ -479,7 +479,7 @@ def extras_measurement(dev, reps=240, n_sets=3):
     top-8, I=768), each launched back to back over three sets of inputs AND
     outputs (each set larger than half of L2, so every launch reads from and
     writes back to HBM): MXFP8 SwiGLU and expand against their bfloat16
-    versions; one tensor-parallel rank's local routing (experts [0, 32) of
+    versions, and the bfloat16 combine; one tensor-parallel rank's local routing (experts [0, 32) of
     128, segments padded to 128 rows) with its padded expand and partial
     combine; and the QK RMSNorm of a Qwen3-30B-A3B-like attention layer
     (T=8192, 32 q heads, 4 k heads, head_dim 128, in place). GB/s =
@@ -539,6 +539,9 @@ def extras_measurement(dev, reps=240, n_sets=3):
                          4 * S * I + S * I + S * I // 32),
         "expand_bf16": ([lambda d=d: lib.moe_expand(p(d["x"]), T, H, k, p(d["r"].inv_perm), p(d["ex"]), sp)
                          for d in sets], 2 * T * H + 2 * S * H + 4 * S),
+        "combine_bf16": ([lambda d=d: lib.moe_combine(p(d["expert_out"]), T, H, k, p(d["r"].topk_weights),
+                                                      p(d["r"].inv_perm), p(d["out"]), sp) for d in sets],
+                         2 * S * H + 8 * S + 2 * T * H),
         "expand_mxfp8": ([lambda d=d: lib.moe_expand_mxfp8(p(d["x"]), T, H, k, p(d["r"].inv_perm), S,
                                                            p(d["ex_c"]), p(d["ex_s"]), sp) for d in sets],
                          2 * T * H + S * H + S * H // 32 + 4 * S),
