@@ -64,3 +64,35 @@ def test_qk_rmsnorm_zero_heads_and_eps(dev, oracle_mod):
     torch.cuda.synchronize()
     check_bf16_close(u16(qd), O.qk_norm(q, k, w, w, 1.0, 3.0)[0], "zero heads")
     assert np.all(O.bf16_decode(u16(kd)) == np.tile([0.5, -0.5], hd // 2))   # 1/sqrt(1+3)
+
+
+@pytest.mark.parametrize("hd", [64, 128, 256])
+def test_qk_rmsnorm_16_byte_aligned_buffers(dev, oracle_mod, hd):
+    """q, k and the weights 16 but not 32 bytes aligned: the 16-byte-vector
+    shape of the kernel, against the oracle."""
+    from memory_bound_moe_gb300 import moe_qk_rmsnorm
+    O = oracle_mod
+    rng = np.random.default_rng(hd)
+    T, nq, nk = 37, 6, 2
+    q = O.bf16_round(rng.standard_normal((T, nq, hd)))
+    k = O.bf16_round(rng.standard_normal((T, nk, hd)) * 2)
+    qw = O.bf16_round(rng.standard_normal(hd) * 0.5)
+    kw = O.bf16_round(rng.standard_normal(hd) * 0.5)
+
+    def shifted(a):   # a device copy that starts 16 bytes past a 256-byte boundary
+        flat = bf16_dev(a.reshape(-1), dev)
+        buf = torch.empty(flat.numel() + 8, dtype=torch.bfloat16, device=dev)
+        view = buf[8:8 + flat.numel()]
+        view.copy_(flat)
+        assert view.data_ptr() % 32 == 16
+        return buf, view.view(a.shape)
+
+    _, qd = shifted(q)
+    _, kd = shifted(k)
+    _, qwd = shifted(qw)
+    _, kwd = shifted(kw)
+    moe_qk_rmsnorm(qd, kd, qwd, kwd, 0.0, 1e-6)
+    torch.cuda.synchronize()
+    rq, rk = O.qk_norm(q, k, qw, kw, 0.0, 1e-6)
+    check_bf16_close(u16(qd), rq, f"q hd={hd} (16-byte aligned)")
+    check_bf16_close(u16(kd), rk, f"k hd={hd} (16-byte aligned)")
