@@ -48,13 +48,6 @@ __device__ __forceinline__ void ld_coherent(Bits<16>& v, const void* p) {
                  : "l"(p));
 }
 
-__device__ __forceinline__ void ld_coherent(Bits<32>& v, const void* p) {
-    asm volatile("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
-                   "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
-                 : "l"(p));
-}
-
 __device__ __forceinline__ void st_global(void* p, const Bits<16>& v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])

@@ -22,6 +22,14 @@
 namespace moe {
 namespace {
 
+// 256-bit coherent load (no L1 allocation): the data is rewritten in place.
+__device__ __forceinline__ void ld_coherent(Bits<32>& v, const void* p) {
+    asm volatile("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]),
+                   "=r"(v.w[4]), "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                 : "l"(p));
+}
+
 template <int HD, int VB, int U, int NT>
 __global__ void __launch_bounds__(NT) qk_norm_kernel(uint8_t* __restrict__ q, uint8_t* __restrict__ k,
                                                      int nq, int nk, uint32_t heads, DivU32 per_token,
