@@ -45,10 +45,19 @@ __global__ void __launch_bounds__(NT) route_rank_kernel(RouteArgs a) {
     extern __shared__ int32_t smem[];
     int32_t* s_cnt = smem;                         // [NW][nloc]
     int32_t* s_tot = s_cnt + (size_t)NW * a.nloc;  // [Ep]
-    pdl_wait_and_release();
-    zero_warp_counters(s_cnt, a.nloc);
     const int t0 = blockIdx.x * a.tpc;
     const int t1 = min(a.T, t0 + a.tpc);
+    // Warm L2 with this block's logit rows before waiting for the kernel
+    // that produced them (a prefetch carries no data into the kernel).
+    if (a.vec4 && t1 > t0) {
+        constexpr uint64_t kPiece = 16384;
+        const uint8_t* base = reinterpret_cast<const uint8_t*>(a.logits + (size_t)t0 * a.E);
+        const uint64_t bytes = uint64_t(t1 - t0) * a.E * sizeof(float);
+        for (uint64_t off = uint64_t(threadIdx.x) * kPiece; off < bytes; off += uint64_t(NT) * kPiece)
+            prefetch_l2(base + off, uint32_t(min(kPiece, bytes - off)));
+    }
+    pdl_wait_and_release();
+    zero_warp_counters(s_cnt, a.nloc);
     int re[kRegRounds], rr[kRegRounds];
     topk_rank_range<GS, EPL, NT, LOCAL>(a, t0, t1, s_cnt, re, rr);
     __syncthreads();
