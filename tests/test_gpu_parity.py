@@ -356,6 +356,8 @@ ROUTE_EXPAND_CASES = [
     (1, 8, 2, 64, True), (7, 3, 3, 24, True), (16, 256, 8, 7168, False), (32, 64, 4, 2880, True),
     (64, 8, 2, 256, True), (128, 8, 8, 16, False), (5, 1024, 16, 512, True), (30, 16, 5, 8, True),
     (33, 64, 4, 256, True), (1023, 32, 4, 2880, True),       # two-kernel route + expand
+    (4096, 128, 8, 2048, True), (8192, 8, 2, 4096, True), (2000, 1024, 16, 64, False),
+    (777, 99, 6, 200, True), (300, 16, 3, 136, False),
 ]
 
 
