@@ -352,6 +352,110 @@ void oracle_quant_mxfp8(const uint16_t* in, long rows, int n, uint8_t* codes, ui
 }
 
 /* ---------------------------------------------------------------------- */
+/* FP4 block quantization: MXFP4 and NVFP4 (E2M1 elements)                 */
+/* ---------------------------------------------------------------------- */
+
+/* Same page and section as MXFP8: the pages name MXFP4 and NVFP4 and their
+ * block sizes (32 and 16 values) but give no formulas. Definitions followed:
+ *  - E2M1, the FP4 element of the OCP Microscaling v1.0 specification: a
+ *    sign bit, 2 exponent bits with bias 1 and 1 mantissa bit, so the code
+ *    c = 0..7 of a magnitude is its index in {0, 0.5, 1, 1.5, 2, 3, 4, 6};
+ *    no infinity or NaN. A real converts to the nearest magnitude, ties to
+ *    the even code (mantissa bit 0), saturating to 6; the sign bit (0x8) is
+ *    the sign of the real, so a negative value that rounds to 0 is -0.
+ *  - MXFP4 (OCP MX v1.0): 32 values share X = floor(log2 amax) - 2 (2: the
+ *    largest E2M1 exponent), clamped to [-127, 127] (-127 when amax = 0),
+ *    stored as the E8M0 byte X + 127; code_i = E2M1(v_i / 2^X).
+ *  - NVFP4 (NVIDIA's published format): 16 values share an E4M3 scale and
+ *    the tensor a float32 scale g > 0. The block scale byte is
+ *    E4M3(fl(fl(g * amax) / 6)) with value s, and code_i = E2M1(fl(v_i * q))
+ *    with q = fl(g / s) (q = 0 when s = 0); a code decodes as E2M1 * s / g.
+ *    fl() is one float32 rounding to nearest even: these steps decide codes,
+ *    so they are taken in float32 here as in the kernels.
+ * Codes are packed two per byte, element 2i in the low nibble. */
+
+static uint8_t e2m1_round(double v) {
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    uint8_t sign = signbit(v) ? (uint8_t)0x8 : (uint8_t)0;
+    double a = fabs(v);
+    if (a >= 6.0) return (uint8_t)(sign | 7);
+    int i = 0;
+    while (i < 7 && mag[i + 1] <= a) ++i;    /* mag[i] <= a < mag[i + 1] */
+    if (a == mag[i]) return (uint8_t)(sign | i);
+    double d0 = a - mag[i], d1 = mag[i + 1] - a;
+    int c;
+    if (d0 < d1) c = i;
+    else if (d1 < d0) c = i + 1;
+    else c = (i % 2 == 0) ? i : i + 1;       /* tie: the even code */
+    return (uint8_t)(sign | c);
+}
+
+void oracle_e2m1_round(const double* in, long n, uint8_t* out) {
+    for (long i = 0; i < n; ++i) out[i] = e2m1_round(in[i]);
+}
+
+static void put_nibble(uint8_t* codes, long idx, uint8_t c) {
+    if (idx % 2 == 0) codes[idx / 2] = (uint8_t)((codes[idx / 2] & 0xF0) | c);
+    else codes[idx / 2] = (uint8_t)((codes[idx / 2] & 0x0F) | (c << 4));
+}
+
+/* MXFP4 of a [rows, n] bfloat16 matrix (n a multiple of 32): codes
+ * [rows, n/2] bytes, scales [rows, n/32] E8M0 bytes. */
+void oracle_quant_mxfp4(const uint16_t* in, long rows, int n, uint8_t* codes, uint8_t* scales) {
+    for (long r = 0; r < rows; ++r) {
+        for (int b = 0; b < n / 32; ++b) {
+            const uint16_t* v = in + r * (long)n + b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                double a = fabs(bf16_to_double(v[i]));
+                if (a > amax) amax = a;
+            }
+            int x;
+            if (amax == 0.0) {
+                x = -127;
+            } else {
+                int e2;
+                (void)frexp(amax, &e2);          /* floor(log2(amax)) = e2 - 1 */
+                x = (e2 - 1) - 2;
+                if (x < -127) x = -127;
+                if (x > 127) x = 127;
+            }
+            scales[r * (long)(n / 32) + b] = (uint8_t)(x + 127);
+            for (int i = 0; i < 32; ++i)
+                put_nibble(codes + r * (long)(n / 2), (long)b * 32 + i,
+                           e2m1_round(ldexp(bf16_to_double(v[i]), -x)));
+        }
+    }
+}
+
+/* NVFP4 of a [rows, n] bfloat16 matrix (n a multiple of 16) with tensor
+ * scale g: codes [rows, n/2] bytes, scales [rows, n/16] E4M3 bytes. */
+void oracle_quant_nvfp4(const uint16_t* in, long rows, int n, float g, uint8_t* codes, uint8_t* scales) {
+    for (long r = 0; r < rows; ++r) {
+        for (int b = 0; b < n / 16; ++b) {
+            const uint16_t* v = in + r * (long)n + b * 16;
+            float amax = 0.0f;                   /* bfloat16 values are exact in float */
+            for (int i = 0; i < 16; ++i) {
+                float a = (float)fabs(bf16_to_double(v[i]));
+                if (a > amax) amax = a;
+            }
+            volatile float t = g * amax;         /* fl(g * amax) */
+            volatile float u = t / 6.0f;         /* fl(t / 6) */
+            uint8_t sb = e4m3_round((double)u);
+            scales[r * (long)(n / 16) + b] = sb;
+            /* decode the (non-negative) E4M3 scale byte */
+            int e = (sb >> 3) & 0xF, m = sb & 7;
+            double s = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+            volatile float q = s > 0.0 ? g / (float)s : 0.0f;   /* fl(g / s) */
+            for (int i = 0; i < 16; ++i) {
+                volatile float p = (float)bf16_to_double(v[i]) * q;   /* fl(v * q) */
+                put_nibble(codes + r * (long)(n / 2), (long)b * 16 + i, e2m1_round((double)p));
+            }
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------- */
 /* Combine: weighted sum of each token's k expert rows                     */
 /* ---------------------------------------------------------------------- */
 

@@ -71,6 +71,14 @@ def _load():
         lib.oracle_quant_mxfp8.argtypes = [_u16p, ctypes.c_long, ctypes.c_int,
                                            ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_uint8)]
         lib.oracle_quant_mxfp8.restype = None
+        lib.oracle_e2m1_round.argtypes = [_f64p, ctypes.c_long, ctypes.POINTER(ctypes.c_uint8)]
+        lib.oracle_e2m1_round.restype = None
+        lib.oracle_quant_mxfp4.argtypes = [_u16p, ctypes.c_long, ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_uint8)]
+        lib.oracle_quant_mxfp4.restype = None
+        lib.oracle_quant_nvfp4.argtypes = [_u16p, ctypes.c_long, ctypes.c_int, ctypes.c_float,
+                                           ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_uint8)]
+        lib.oracle_quant_nvfp4.restype = None
         lib.oracle_rmsnorm_heads.argtypes = [_u16p, ctypes.c_long, ctypes.c_int, _u16p, ctypes.c_double,
                                              ctypes.c_double, _u16p]
         lib.oracle_rmsnorm_heads.restype = None
@@ -283,6 +291,78 @@ def dequant_mxfp8(codes, scales) -> np.ndarray:
     rows, n = codes.shape
     x = np.asarray(scales).astype(np.float64) - 127.0
     return e4m3_decode(codes) * np.repeat(2.0 ** x, 32, axis=1).reshape(rows, n)
+
+
+def e2m1_round(v) -> np.ndarray:
+    """Round reals to E2M1 codes 0..15 (nearest, ties to the even code,
+    saturating to +-6, sign kept)."""
+    v = _c(v, np.float64)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e2m1_round(_ptr(v, ctypes.c_double), v.size, _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def e2m1_decode(c) -> np.ndarray:
+    """E2M1 codes (0..15) -> float64, from the format's definition: sign bit
+    0x8, exponent bits 0x6 with bias 1, mantissa bit 0x1 (exponent 0 is
+    subnormal: 0.m * 2^0)."""
+    c = np.asarray(c, dtype=np.uint8)
+    sign = np.where(c & 0x8, -1.0, 1.0)
+    e = ((c >> 1) & 0x3).astype(np.float64)
+    m = (c & 1).astype(np.float64)
+    val = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * 2.0 ** (e - 1.0))
+    return sign * val
+
+
+def unpack_fp4(codes) -> np.ndarray:
+    """[rows, n/2] bytes -> [rows, n] codes (element 2i in the low nibble)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    out = np.empty(codes.shape[:-1] + (codes.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = codes & 0x0F
+    out[..., 1::2] = codes >> 4
+    return out
+
+
+def quant_mxfp4(x_bf16):
+    """MXFP4 of a [rows, n] bfloat16 matrix (n % 32 == 0): returns (codes
+    uint8 [rows, n/2], two per byte, scales uint8 [rows, n/32] E8M0)."""
+    x = _c(x_bf16, np.uint16)
+    rows, n = x.shape
+    assert n % 32 == 0
+    codes = np.zeros((rows, n // 2), dtype=np.uint8)
+    scales = np.empty((rows, n // 32), dtype=np.uint8)
+    _load().oracle_quant_mxfp4(_ptr(x, ctypes.c_uint16), rows, n, _ptr(codes, ctypes.c_uint8),
+                               _ptr(scales, ctypes.c_uint8))
+    return codes, scales
+
+
+def dequant_mxfp4(codes, scales) -> np.ndarray:
+    """E2M1(code) * 2^(scale - 127), float64, [rows, n]."""
+    c = unpack_fp4(codes)
+    rows, n = c.shape
+    x = np.asarray(scales).astype(np.float64) - 127.0
+    return e2m1_decode(c) * np.repeat(2.0 ** x, 32, axis=1).reshape(rows, n)
+
+
+def quant_nvfp4(x_bf16, global_scale: float):
+    """NVFP4 of a [rows, n] bfloat16 matrix (n % 16 == 0) with tensor scale
+    g > 0: returns (codes uint8 [rows, n/2], scales uint8 [rows, n/16] E4M3)."""
+    x = _c(x_bf16, np.uint16)
+    rows, n = x.shape
+    assert n % 16 == 0
+    codes = np.zeros((rows, n // 2), dtype=np.uint8)
+    scales = np.empty((rows, n // 16), dtype=np.uint8)
+    _load().oracle_quant_nvfp4(_ptr(x, ctypes.c_uint16), rows, n, float(global_scale),
+                               _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8))
+    return codes, scales
+
+
+def dequant_nvfp4(codes, scales, global_scale: float) -> np.ndarray:
+    """E2M1(code) * E4M3(scale) / g, float64, [rows, n]."""
+    c = unpack_fp4(codes)
+    rows, n = c.shape
+    s = e4m3_decode(scales)
+    return e2m1_decode(c) * np.repeat(s / float(global_scale), 16, axis=1).reshape(rows, n)
 
 
 def rmsnorm_heads(x, w, bias: float, eps: float) -> np.ndarray:

@@ -548,6 +548,148 @@ def test_mxfp8_round_trip_error_bound(oracle_mod):
 
 
 # ---------------------------------------------------------------------------
+# FP4 (E2M1) block quantization: MXFP4 and NVFP4
+# ---------------------------------------------------------------------------
+
+# The E2M1 value of every code, as tabulated by the OCP Microscaling v1.0
+# specification (sign bit 0x8; exponent bias 1; 0.5 is the one subnormal).
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def test_e2m1_decode_table(oracle_mod):
+    got = oracle_mod.e2m1_decode(np.arange(16, dtype=np.uint8))
+    assert got.tolist() == E2M1_TABLE
+    assert np.all(np.signbit(got[8:]))
+
+
+def test_e2m1_round_known_patterns(oracle_mod):
+    cases = [  # value, code: exact values, ties to the even code, saturation, sign
+        (0.0, 0x0), (0.5, 0x1), (1.0, 0x2), (1.5, 0x3), (2.0, 0x4), (3.0, 0x5), (4.0, 0x6), (6.0, 0x7),
+        (0.25, 0x0), (0.75, 0x2), (1.25, 0x2), (1.75, 0x4), (2.5, 0x4), (3.5, 0x6), (5.0, 0x6),
+        (0.2499, 0x0), (0.2501, 0x1), (0.7499, 0x1), (0.7501, 0x2), (2.4999, 0x4), (2.5001, 0x5),
+        (4.9999, 0x6), (5.0001, 0x7), (7.0, 0x7), (100.0, 0x7), (1e-30, 0x0),
+        (-0.1, 0x8), (-0.0, 0x8), (-0.3, 0x9), (-1.0, 0xA), (-5.0, 0xE), (-6.0, 0xF), (-1e9, 0xF),
+    ]
+    got = oracle_mod.e2m1_round(np.array([v for v, _ in cases]))
+    assert got.tolist() == [c for _, c in cases]
+
+
+def test_e2m1_round_is_nearest_with_even_ties(oracle_mod):
+    """Brute force: the nearest of the 8 magnitudes (the even code on a tie),
+    for a sweep that hits every midpoint."""
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    rng = np.random.default_rng(7)
+    v = np.concatenate([rng.uniform(-7.5, 7.5, 20000), np.arange(-6.5, 6.5001, 0.125)])
+    got = oracle_mod.e2m1_round(v)
+    for x, c in zip(v, got):
+        d = np.abs(np.abs(x) - mags)
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        if abs(x) >= 6:
+            want = 7
+        assert c == (want | (0x8 if np.signbit(x) else 0)), (x, c, want)
+
+
+def test_fp4_nibble_packing(oracle_mod):
+    O = oracle_mod
+    x = O.bf16_round(np.array([[1.0, 6.0, -0.5, 2.0] + [0.0] * 28]))   # amax 6: X = 0
+    codes, scales = O.quant_mxfp4(x)
+    assert scales.tolist() == [[127]]
+    assert codes[0, :2].tolist() == [0x72, 0x49]    # element 2i in the low nibble
+
+
+def test_mxfp4_scales_closed_forms(oracle_mod):
+    O = oracle_mod
+    rows = np.zeros((5, 64))
+    rows[0, :32] = 6.0                        # amax 6: X = floor(log2 6) - 2 = 0, codes 0x7
+    rows[0, 32:] = 0.0                        # zero block: X = -127, byte 0, codes 0
+    rows[1, :32] = 1.0                        # amax 1: X = -2, 1 * 4 = 4 -> 0x6
+    rows[1, 32:] = np.linspace(-0.75, 0.75, 32)   # amax 0.75: X = -3
+    rows[2, :32] = 2.0 ** -130                # X clamps to -127: 2^-3 rounds to 0
+    rows[2, 32:] = 7.0                        # amax 7: X = 0; 7 saturates to 6
+    rows[3, :] = np.arange(64) - 31.5         # amax 31.5 / 32: X = 2
+    rows[4, :] = 3.0e38                       # top of the bf16 range: X = 127 - 2
+    x = O.bf16_round(rows)
+    codes, scales = O.quant_mxfp4(x)
+    assert scales.tolist() == [[127, 0], [125, 124], [0, 127], [129, 129], [252, 252]]
+    c = O.unpack_fp4(codes)
+    assert np.all(c[0, :32] == 0x7) and np.all(c[0, 32:] == 0)
+    assert np.all(c[1, :32] == 0x6)
+    assert np.all(c[2, :32] == 0x0) and np.all(c[2, 32:] == 0x7)
+    # 0.75 * 2^3 = 6 -> 0x7 at the ends of the linspace block
+    assert c[1, 32] == 0xF and c[1, 63] == 0x7
+
+
+def test_mxfp4_round_trip_error_bound(oracle_mod):
+    O = oracle_mod
+    rng = np.random.default_rng(2)
+    v = rng.standard_normal((64, 256)) * np.exp(rng.uniform(-12, 12, (64, 1)))
+    x = O.bf16_round(v)
+    xv = O.bf16_decode(x)
+    codes, scales = O.quant_mxfp4(x)
+    deq = O.dequant_mxfp4(codes, scales)
+    X = np.repeat(scales.astype(np.float64) - 127, 32, axis=1)
+    scaled = np.abs(xv) / 2.0 ** X
+    amax_scaled = scaled.reshape(64, 8, 32).max(axis=2)
+    assert np.all((amax_scaled >= 4) & (amax_scaled < 8))   # amax lands in [4, 8)
+    inside = scaled <= 6
+    # half the E2M1 spacing: at most 1 (between 4 and 6), in units of 2^X
+    assert np.all(np.abs(deq - xv)[inside] <= 2.0 ** X[inside])
+    assert np.all(np.abs(deq[~inside]) == 6 * 2.0 ** X[~inside])
+    assert np.all(np.sign(deq) * np.sign(xv) >= 0)
+
+
+def test_nvfp4_closed_forms(oracle_mod):
+    O = oracle_mod
+    rows = np.zeros((3, 32))
+    rows[0, :16] = [6.0, -3.0, 1.0, 0.5] + [0.0] * 12   # g = 1: scale E4M3(1) = 0x38, codes = E2M1(v)
+    rows[0, 16:] = 0.0                                  # zero block: scale 0, codes 0
+    rows[1, :16] = 12.0                                 # g = 1: t = 12/6 = 2 -> 0x40; v * 1/2 = 6
+    rows[1, 16:] = np.linspace(-3.0, 3.0, 16)           # amax 3: scale E4M3(0.5) = 0x30
+    rows[2, :] = 1000.0                                 # g = 1: 1000/6 = 166.67 -> E4M3 160 = 1.25 * 2^7 (0x72)
+    x = O.bf16_round(rows)
+    codes, scales = O.quant_nvfp4(x, 1.0)
+    assert scales.tolist() == [[0x38, 0x00], [0x40, 0x30], [0x72, 0x72]]
+    c = O.unpack_fp4(codes)
+    assert c[0, :4].tolist() == [0x7, 0xD, 0x2, 0x1] and np.all(c[0, 4:] == 0)
+    assert np.all(c[1, :16] == 0x7)
+    assert c[1, 16] == 0xF and c[1, 31] == 0x7            # +-3 / 0.5 = +-6
+    # 1000 * (1 / 160) = 6.25 saturates to 6
+    assert np.all(c[2] == 0x7)
+    # a calibrated tensor scale g = 448 * 6 / amax puts the largest block's
+    # scale at E4M3's top (448) and its largest value at code 6
+    xv = O.bf16_decode(x[1:2])
+    g = 448.0 * 6.0 / np.abs(xv).max()
+    codes, scales = O.quant_nvfp4(x[1:2], g)
+    assert scales[0, 0] == 0x7E and np.all(O.unpack_fp4(codes)[0, :16] == 0x7)
+
+
+@pytest.mark.parametrize("g", [1.0, 0.37, 448.0 * 6.0 / 9.0])
+def test_nvfp4_round_trip_error_bound(oracle_mod, g):
+    O = oracle_mod
+    rng = np.random.default_rng(3)
+    v = rng.standard_normal((32, 128)) * np.exp(rng.uniform(-3, 3, (32, 1)))
+    x = O.bf16_round(v)
+    xv = O.bf16_decode(x)
+    codes, scales = O.quant_nvfp4(x, g)
+    deq = O.dequant_nvfp4(codes, scales, g)
+    s = np.repeat(O.e4m3_decode(scales), 16, axis=1)
+    unit = s / g                      # the value of E2M1 1.0 in this block
+    scaled = np.abs(xv) / unit
+    inside = scaled <= 6
+    # within half the largest E2M1 spacing (1 unit); beyond 6 units, saturated
+    assert np.all(np.abs(deq - xv)[inside] <= unit[inside] * (1 + 1e-6))
+    assert np.all(np.abs(deq[~inside]) == 6 * unit[~inside])
+    # where g * amax / 6 lies in E4M3's normal range (2^-6 .. 448), its
+    # rounding is within 2^-4 relative, so the block's largest value lands
+    # at most 6 / (1 - 2^-4) after scaling
+    raw = g * np.abs(xv).reshape(32, 8, 16).max(axis=2) / 6
+    normal = np.repeat((raw >= 2.0 ** -6) & (raw <= 448), 16, axis=1)
+    assert np.all(scaled[normal] <= 6 / (1 - 2.0 ** -4) * (1 + 1e-6))
+    assert np.all(np.sign(deq) * np.sign(xv) >= 0)
+
+
+# ---------------------------------------------------------------------------
 # QK RMSNorm
 # ---------------------------------------------------------------------------
 
