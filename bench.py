@@ -479,7 +479,8 @@ def extras_measurement(dev, reps=240, n_sets=3):
     top-8, I=768), each launched back to back over three sets of inputs AND
     outputs (each set larger than half of L2, so every launch reads from and
     writes back to HBM): MXFP8 SwiGLU and expand against their bfloat16
-    versions, and the bfloat16 combine; one tensor-parallel rank's local routing (experts [0, 32) of
+    versions, NVFP4 (tensor scale 64) and MXFP4 SwiGLU and expand, and the
+    bfloat16 combine; one tensor-parallel rank's local routing (experts [0, 32) of
     128, segments padded to 128 rows) with its padded expand and partial
     combine; and the QK RMSNorm of a Qwen3-30B-A3B-like attention layer
     (T=8192, 32 q heads, 4 k heads, head_dim 128, in place). GB/s =
@@ -506,6 +507,8 @@ def extras_measurement(dev, reps=240, n_sets=3):
         d["act_c"], d["act_s"] = torch.empty((S, I), **u8), torch.empty((S, I // 32), **u8)
         d["ex"] = torch.empty((S, H), **bf)
         d["ex_c"], d["ex_s"] = torch.empty((S, H), **u8), torch.empty((S, H // 32), **u8)
+        d["act4"], d["ex4"] = torch.empty((S, I // 2), **u8), torch.empty((S, H // 2), **u8)
+        d["act4_s"], d["ex4_s"] = torch.empty((S, I // 16), **u8), torch.empty((S, H // 16), **u8)
         d["loc"] = moe.moe_route_local(d["logits"], k, True, e0, e1, pad)
         d["lex"] = torch.empty((rows, H), **bf)
         d["leo"] = torch.randn((rows, H), device=dev).to(torch.bfloat16)
@@ -545,6 +548,18 @@ def extras_measurement(dev, reps=240, n_sets=3):
         "expand_mxfp8": ([lambda d=d: lib.moe_expand_mxfp8(p(d["x"]), T, H, k, p(d["r"].inv_perm), S,
                                                            p(d["ex_c"]), p(d["ex_s"]), sp) for d in sets],
                          2 * T * H + S * H + S * H // 32 + 4 * S),
+        "swiglu_nvfp4": ([lambda d=d: lib.moe_swiglu_fp4(p(d["gate_up"]), S, I, 0, 64.0, p(d["act4"]),
+                                                        p(d["act4_s"]), sp) for d in sets],
+                         4 * S * I + S * I // 2 + S * I // 16),
+        "swiglu_mxfp4": ([lambda d=d: lib.moe_swiglu_fp4(p(d["gate_up"]), S, I, 1, 0.0, p(d["act4"]),
+                                                        p(d["act4_s"]), sp) for d in sets],
+                         4 * S * I + S * I // 2 + S * I // 32),
+        "expand_nvfp4": ([lambda d=d: lib.moe_expand_fp4(p(d["x"]), T, H, k, p(d["r"].inv_perm), S, 0, 64.0,
+                                                        p(d["ex4"]), p(d["ex4_s"]), sp) for d in sets],
+                         2 * T * H + S * H // 2 + S * H // 16 + 4 * S),
+        "expand_mxfp4": ([lambda d=d: lib.moe_expand_fp4(p(d["x"]), T, H, k, p(d["r"].inv_perm), S, 1, 0.0,
+                                                        p(d["ex4"]), p(d["ex4_s"]), sp) for d in sets],
+                         2 * T * H + S * H // 2 + S * H // 32 + 4 * S),
         "route_local_rank0of4": ([lambda d=d: lib.moe_route_local(
             p(d["logits"]), T, E, k, 1, e0, e1, pad, p(d["loc"].topk_ids), p(d["loc"].topk_weights),
             p(d["loc"].expert_counts), p(d["loc"].expert_offsets), p(d["loc"].perm), p(d["loc"].inv_perm),

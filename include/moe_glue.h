@@ -320,6 +320,46 @@ moe_status_t moe_expand_mxfp8(const moe_bf16_t* x, int64_t T, int H, int k,
                               uint8_t* codes, uint8_t* scales, moe_stream_t stream);
 
 /*
+ * FP4 outputs for the next expert GEMM, fused into SwiGLU and row expansion.
+ * "CuTeDSL at Perplexity", section "Blackwell support": besides MXFP8,
+ * Blackwell supports MXFP4 and NVFP4 in hardware, and the kernels compute
+ * the absolute maximum over 32 (MXFP4) or 16 (NVFP4) values with sub-warp
+ * reductions. Element: E2M1 (OCP Microscaling v1.0; magnitudes 0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6), a real rounded to nearest, ties to the even code,
+ * saturating to +-6, sign kept (a negative value rounding to 0 is code 0x8).
+ *
+ *   MOE_FP4_MXFP4 (OCP MX v1.0): per 32 values with largest magnitude amax,
+ *     X = floor(log2 amax) - 2 clamped to [-127, 127] (-127 if amax = 0);
+ *     scale byte (E8M0) = X + 127; code = E2M1(v * 2^-X); value = E2M1 * 2^X.
+ *     global_scale is ignored.
+ *   MOE_FP4_NVFP4 (NVIDIA's format): per 16 values, with the float32 tensor
+ *     scale g = global_scale (finite, > 0; e.g. 448 * 6 / the tensor's amax),
+ *     scale byte (E4M3) = E4M3(fl(fl(g * amax) / 6)) of value s, round to
+ *     nearest even, saturating to 448; code = E2M1(fl(v * fl(g / s))), 0 if
+ *     s = 0; fl() is one float32 rounding. value = E2M1 * s / g.
+ *
+ * codes [rows, n/2] bytes, two codes per byte, element 2i in the LOW nibble
+ * (16-byte aligned); scales [rows, n/32] (MXFP4) or [rows, n/16] (NVFP4)
+ * bytes; both row-major. n (I or H) must be a multiple of the block
+ * (MOE_ERR_MISALIGNED); an unknown format or a bad NVFP4 scale is
+ * MOE_ERR_INVALID_ARG. The values quantized are the bfloat16 values
+ * moe_swiglu / moe_expand would store. Inputs are assumed finite.
+ *
+ * moe_swiglu_fp4: act = silu(gate) * up as moe_swiglu, then quantized.
+ * moe_expand_fp4: token rows quantized once and written to the k rows
+ *   inv_perm[t*k + j] < rows (rows as for moe_expand_rows).
+ */
+#define MOE_FP4_NVFP4 0
+#define MOE_FP4_MXFP4 1
+moe_status_t moe_swiglu_fp4(const moe_bf16_t* gate_up, int64_t rows, int I, int format,
+                            float global_scale, uint8_t* act_codes, uint8_t* act_scales,
+                            moe_stream_t stream);
+moe_status_t moe_expand_fp4(const moe_bf16_t* x, int64_t T, int H, int k,
+                            const int32_t* inv_perm, int64_t rows, int format,
+                            float global_scale, uint8_t* codes, uint8_t* scales,
+                            moe_stream_t stream);
+
+/*
  * QK RMSNorm, in place, for the attention layer of the same models.
  * "CuTeDSL at Perplexity", section "QK normalization": recent Qwen models
  * normalise every head of q and of k (64, 128 or 256 elements) with RMS

@@ -13,10 +13,11 @@ from .binding import (MoeError, RouteResult, STATUS, library_path, load_library,
                       moe_combine_rows, moe_expand, moe_expand_rows, moe_route, moe_route_expand,
                       moe_route_local, moe_route_local_rows, moe_route_local_workspace_size,
                       moe_route_workspace_size, moe_status_string, moe_swiglu,
-                      moe_swiglu_mxfp8, moe_expand_mxfp8, moe_qk_rmsnorm)
+                      moe_swiglu_mxfp8, moe_expand_mxfp8, moe_swiglu_fp4, moe_expand_fp4,
+                      moe_qk_rmsnorm)
 
 __all__ = ["MoeError", "RouteResult", "STATUS", "library_path", "load_library", "moe_combine",
            "moe_combine_rows", "moe_expand", "moe_expand_rows", "moe_route", "moe_route_expand",
            "moe_route_local", "moe_route_local_rows", "moe_route_local_workspace_size",
            "moe_route_workspace_size", "moe_status_string", "moe_swiglu",
-           "moe_swiglu_mxfp8", "moe_expand_mxfp8", "moe_qk_rmsnorm"]
+           "moe_swiglu_mxfp8", "moe_expand_mxfp8", "moe_swiglu_fp4", "moe_expand_fp4", "moe_qk_rmsnorm"]

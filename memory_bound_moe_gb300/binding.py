@@ -76,6 +76,10 @@ def load_library():
         lib.moe_swiglu_mxfp8.restype = _int
         lib.moe_expand_mxfp8.argtypes = [_vp, _i64, _int, _int, _vp, _i64, _vp, _vp, _vp]
         lib.moe_expand_mxfp8.restype = _int
+        lib.moe_swiglu_fp4.argtypes = [_vp, _i64, _int, _int, ctypes.c_float, _vp, _vp, _vp]
+        lib.moe_swiglu_fp4.restype = _int
+        lib.moe_expand_fp4.argtypes = [_vp, _i64, _int, _int, _vp, _i64, _int, ctypes.c_float, _vp, _vp, _vp]
+        lib.moe_expand_fp4.restype = _int
         lib.moe_qk_rmsnorm.argtypes = [_vp, _vp, _i64, _int, _int, _int, _vp, _vp, ctypes.c_float,
                                        ctypes.c_float, _vp]
         lib.moe_qk_rmsnorm.restype = _int
@@ -414,6 +418,62 @@ def moe_expand_mxfp8(x: torch.Tensor, inv_perm: torch.Tensor, k: int, rows: Opti
     _check("moe_expand_mxfp8", load_library().moe_expand_mxfp8(_ptr(x), T, H, int(k), _ptr(inv_perm), rows,
                                                                _ptr(codes), _ptr(scales),
                                                                _stream_ptr(stream, dev)))
+    return codes, scales
+
+
+FP4_FORMATS = {"nvfp4": (0, 16), "mxfp4": (1, 32)}   # C-ABI format code, values per scale
+
+
+def _fp4(fmt: str):
+    if fmt not in FP4_FORMATS:
+        raise ValueError(f"unknown FP4 format {fmt!r}: expected one of {sorted(FP4_FORMATS)}")
+    return FP4_FORMATS[fmt]
+
+
+def moe_swiglu_fp4(gate_up: torch.Tensor, fmt: str = "nvfp4", global_scale: float = 1.0, *,
+                   codes: Optional[torch.Tensor] = None, scales: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None):
+    """SwiGLU of ``gate_up [rows, 2I]`` quantized to NVFP4 (tensor scale
+    ``global_scale``) or MXFP4: returns ``(codes uint8 [rows, I/2], two per
+    byte, scales uint8 [rows, I/16] E4M3 or [rows, I/32] E8M0)``."""
+    code, block = _fp4(fmt)
+    rows, two_i = gate_up.shape
+    I = two_i // 2
+    _need(gate_up, "gate_up", torch.bfloat16, (rows, two_i))
+    dev = gate_up.device
+    if codes is None:
+        codes = torch.empty((rows, I // 2), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty((rows, I // block), dtype=torch.uint8, device=dev)
+    _need(codes, "act_codes", torch.uint8, (rows, I // 2))
+    _need(scales, "act_scales", torch.uint8, (rows, I // block))
+    _check("moe_swiglu_fp4", load_library().moe_swiglu_fp4(_ptr(gate_up), rows, I, code, float(global_scale),
+                                                           _ptr(codes), _ptr(scales), _stream_ptr(stream, dev)))
+    return codes, scales
+
+
+def moe_expand_fp4(x: torch.Tensor, inv_perm: torch.Tensor, k: int, fmt: str = "nvfp4",
+                   global_scale: float = 1.0, rows: Optional[int] = None, *,
+                   codes: Optional[torch.Tensor] = None, scales: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None):
+    """Expansion of ``x [T, H]`` quantized to NVFP4 or MXFP4 into ``rows``
+    rows (default T*k): returns ``(codes uint8 [rows, H/2], scales uint8
+    [rows, H/16] or [rows, H/32])``."""
+    code, block = _fp4(fmt)
+    T, H = x.shape
+    _need(x, "x", torch.bfloat16, (T, H))
+    _need(inv_perm, "inv_perm", torch.int32, (T * k,))
+    rows = T * k if rows is None else rows
+    dev = x.device
+    if codes is None:
+        codes = torch.empty((rows, H // 2), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty((rows, H // block), dtype=torch.uint8, device=dev)
+    _need(codes, "codes", torch.uint8, (rows, H // 2))
+    _need(scales, "scales", torch.uint8, (rows, H // block))
+    _check("moe_expand_fp4", load_library().moe_expand_fp4(_ptr(x), T, H, int(k), _ptr(inv_perm), rows, code,
+                                                           float(global_scale), _ptr(codes), _ptr(scales),
+                                                           _stream_ptr(stream, dev)))
     return codes, scales
 
 

@@ -414,6 +414,65 @@ moe_status_t moe_expand_mxfp8(const moe_bf16_t* x, int64_t T, int H, int k, cons
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+
+// The FP4 format arguments: a known format, n a multiple of its block, and
+// for NVFP4 a finite positive tensor scale.
+moe_status_t check_fp4(int format, int n, float global_scale) {
+    if (format != MOE_FP4_NVFP4 && format != MOE_FP4_MXFP4) return MOE_ERR_INVALID_ARG;
+    if (format == MOE_FP4_NVFP4 && !(global_scale > 0.0f && global_scale <= 3.4028234663852886e38f))
+        return MOE_ERR_INVALID_ARG;
+    if (n % (format == MOE_FP4_NVFP4 ? 16 : 32) != 0) return MOE_ERR_MISALIGNED;
+    return MOE_OK;
+}
+
+}  // namespace
+
+moe_status_t moe_swiglu_fp4(const moe_bf16_t* gate_up, int64_t rows, int I, int format,
+                            float global_scale, uint8_t* act_codes, uint8_t* act_scales,
+                            moe_stream_t stream) {
+    moe_status_t st = check_rows(rows, I, 1);
+    if (st != MOE_OK) return st;
+    if ((st = check_fp4(format, I, global_scale)) != MOE_OK) return st;
+    if (rows == 0) return MOE_OK;
+    if (gate_up == nullptr || act_codes == nullptr || act_scales == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(gate_up) || !aligned16(act_codes)) return MOE_ERR_MISALIGNED;
+    const uint64_t n = uint64_t(rows) * uint64_t(I);
+    const uint64_t block = format == MOE_FP4_NVFP4 ? 16 : 32;
+    if (any_overlap({{act_codes, n / 2}, {act_scales, n / block}}, {{gate_up, 4 * n}}))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_swiglu_fp4(gate_up, rows, I, format == MOE_FP4_NVFP4, global_scale, act_codes,
+                                            act_scales, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_expand_fp4(const moe_bf16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
+                            int64_t rows, int format, float global_scale, uint8_t* codes,
+                            uint8_t* scales, moe_stream_t stream) {
+    if (k < 1) return MOE_ERR_INVALID_ARG;
+    if (k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
+    moe_status_t st = check_rows(T, H, k);
+    if (st != MOE_OK) return st;
+    if ((st = check_fp4(format, H, global_scale)) != MOE_OK) return st;
+    if (rows < 0) return MOE_ERR_INVALID_ARG;
+    if (rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (T == 0 || rows == 0) return MOE_OK;
+    if (x == nullptr || inv_perm == nullptr || codes == nullptr || scales == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(codes) || !aligned4(inv_perm)) return MOE_ERR_MISALIGNED;
+    const uint64_t S = uint64_t(T) * uint64_t(k);
+    const uint64_t n = uint64_t(rows) * uint64_t(H);
+    const uint64_t block = format == MOE_FP4_NVFP4 ? 16 : 32;
+    if (any_overlap({{codes, n / 2}, {scales, n / block}},
+                    {{x, 2 * uint64_t(T) * uint64_t(H)}, {inv_perm, 4 * S}}))
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(moe::launch_expand_fp4(x, T, H, k, inv_perm, rows, format == MOE_FP4_NVFP4, global_scale,
+                                            codes, scales, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_qk_rmsnorm(moe_bf16_t* q, moe_bf16_t* k, int64_t T, int num_q_heads,
                             int num_k_heads, int head_dim, const moe_bf16_t* q_weight,
                             const moe_bf16_t* k_weight, float weight_bias, float eps,

@@ -67,6 +67,12 @@ cudaError_t launch_swiglu_mxfp8(const uint16_t* gate_up, int64_t rows, int I, ui
 cudaError_t launch_expand_mxfp8(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
                                 int64_t rows, uint8_t* codes, uint8_t* scales, int num_sms,
                                 cudaStream_t stream);
+// FP4 outputs: NVFP4 (nvfp4, tensor scale g) or MXFP4.
+cudaError_t launch_swiglu_fp4(const uint16_t* gate_up, int64_t rows, int I, bool nvfp4, float g,
+                              uint8_t* codes, uint8_t* scales, int num_sms, cudaStream_t stream);
+cudaError_t launch_expand_fp4(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
+                              int64_t rows, bool nvfp4, float g, uint8_t* codes, uint8_t* scales,
+                              int num_sms, cudaStream_t stream);
 
 // Per-head RMSNorm of q [T, nq, head_dim] and k [T, nk, head_dim] in place
 // (qknorm.cu); head_dim 64, 128 or 256.

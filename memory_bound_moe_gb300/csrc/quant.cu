@@ -13,8 +13,19 @@
 // bfloat16 values the unquantized kernels would store, so a block's scale is
 // decided on exactly those values.
 //
-// Layout: codes [rows, n] bytes, row-major (a row is a whole number of 32-byte
-// blocks); scales [rows, n/32] bytes, row-major.
+// The same page names MXFP4 and NVFP4 with 32- and 16-value blocks; their
+// element is E2M1 (OCP MX v1.0: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), from
+// the hardware cvt.rn.satfinite.e2m1x2.f32 (nearest even, saturating, sign
+// kept).
+//  - MXFP4: X = floor(log2 amax) - 2 clamped to [-127, 127], scale byte
+//    X + 127 (E8M0), code = E2M1(v * 2^-X).
+//  - NVFP4 (NVIDIA's format) with a float32 tensor scale g: scale byte
+//    E4M3(fl(fl(g * amax) / 6)) of value s, code = E2M1(fl(v * fl(g / s)))
+//    (0 when s = 0), every step one float32 rounding to nearest even.
+//
+// Layout: codes [rows, n * bits / 8] bytes, row-major, two FP4 codes per byte
+// with element 2i in the low nibble; scales [rows, n / block] bytes,
+// row-major.
 #include "moe_device.cuh"
 #include "moe_launch.h"
 #include "rows_common.cuh"
@@ -30,14 +41,33 @@ __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
     return d;
 }
 
+// Two floats -> one byte of two E2M1 codes (the first argument in the low
+// nibble).
+__device__ __forceinline__ uint32_t pack_e2m1x2(float lo, float hi) {
+    uint16_t d;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// The value of a non-negative E4M3 byte (4 exponent bits with bias 7, 3
+// fraction bits), exactly.
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+    const uint32_t e = (b >> 3) & 0xfu, m = b & 7u;
+    if (e == 0) return float(m) * __uint_as_float(uint32_t(127 - 9) << 23);
+    return float(8u + m) * __uint_as_float((e - 10u + 127u) << 23);
+}
+
 // Shared exponent of a block from its largest magnitude (amax >= 0, a
 // bfloat16 value): floor(log2 amax) is the float's exponent field minus 127
-// for normal values; amax below 2^-119 (zero and subnormal included) clamps to
-// X = -127.
+// for normal values; EMAX is the element format's largest exponent (8 for
+// E4M3, 2 for E2M1); amax below 2^-119 (zero and subnormal included) clamps
+// to X = -127.
+template <int EMAX>
 __device__ __forceinline__ int mx_exponent(float amax) {
     const int ef = int((__float_as_uint(amax) >> 23) & 0xffu);
     if (ef == 0) return -127;
-    return max(min(ef - 127 - 8, 127), -127);
+    return max(min(ef - 127 - EMAX, 127), -127);
 }
 
 // 2^-x for x in [-127, 126] as an exact float.
@@ -45,43 +75,74 @@ __device__ __forceinline__ float exp2_neg(int x) {
     return __uint_as_float(uint32_t(127 - x) << 23);
 }
 
-// EPT consecutive values of one row (EPT = 16 or 8) -> codes; the MX block of
-// 32 spans 32/EPT consecutive lanes (aligned), reduced with xor shuffles. All
-// lanes of the warp must call; `valid` lanes contribute their values.
-template <int EPT>
-struct MxChunk {
-    uint32_t codes[EPT / 4];
-    int x;
+enum Fmt { kMxfp8 = 0, kMxfp4 = 1, kNvfp4 = 2 };
+
+template <int F>
+struct FmtInfo {
+    static constexpr int kBlock = F == kNvfp4 ? 16 : 32;   // values per scale
+    static constexpr int kBits = F == kMxfp8 ? 8 : 4;      // bits per code
 };
 
-template <int EPT>
-__device__ __forceinline__ MxChunk<EPT> quantize_chunk(const float (&v)[EPT], bool valid) {
+// EPT consecutive values of one row (EPT = 16 or 8) -> codes, and the scale
+// byte of their block; a block spans kBlock / EPT consecutive lanes (aligned),
+// reduced with xor shuffles. All lanes of the warp must call; `valid` lanes
+// contribute their values. g: the NVFP4 tensor scale.
+template <int F, int EPT>
+struct QChunk {
+    static constexpr int kWords = EPT * FmtInfo<F>::kBits / 32;
+    uint32_t codes[kWords];
+    uint32_t scale;
+};
+
+template <int F, int EPT>
+__device__ __forceinline__ QChunk<F, EPT> quantize_chunk(const float (&v)[EPT], bool valid, float g) {
+    constexpr int kLanes = FmtInfo<F>::kBlock / EPT;
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < EPT; ++i) amax = fmaxf(amax, fabsf(v[i]));
     if (!valid) amax = 0.0f;
 #pragma unroll
-    for (int o = 1; o < 32 / EPT; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-    MxChunk<EPT> c;
-    c.x = mx_exponent(amax);
-    const float s = exp2_neg(min(c.x, 126));
+    for (int o = 1; o < kLanes; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    QChunk<F, EPT> c;
+    float p[EPT];   // the values the element conversion rounds
+    if constexpr (F == kNvfp4) {
+        const float t = __fdiv_rn(__fmul_rn(g, amax), 6.0f);
+        c.scale = pack_e4m3x2(t, 0.0f) & 0xffu;
+        const float sv = e4m3_value(c.scale);
+        const float q = sv > 0.0f ? __fdiv_rn(g, sv) : 0.0f;
 #pragma unroll
-    for (int q = 0; q < EPT / 4; ++q) {
-        const uint32_t lo = pack_e4m3x2(v[4 * q] * s, v[4 * q + 1] * s);
-        const uint32_t hi = pack_e4m3x2(v[4 * q + 2] * s, v[4 * q + 3] * s);
-        c.codes[q] = lo | (hi << 16);
+        for (int i = 0; i < EPT; ++i) p[i] = __fmul_rn(v[i], q);
+    } else {
+        const int x = mx_exponent<F == kMxfp8 ? 8 : 2>(amax);
+        c.scale = uint32_t(x + 127);
+        const float s = exp2_neg(min(x, 126));
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) p[i] = v[i] * s;   // exact: a power of two
+    }
+    if constexpr (F == kMxfp8) {
+#pragma unroll
+        for (int q = 0; q < EPT / 4; ++q)
+            c.codes[q] = uint32_t(pack_e4m3x2(p[4 * q], p[4 * q + 1])) |
+                         (uint32_t(pack_e4m3x2(p[4 * q + 2], p[4 * q + 3])) << 16);
+    } else {
+#pragma unroll
+        for (int q = 0; q < EPT / 8; ++q)
+            c.codes[q] = pack_e2m1x2(p[8 * q], p[8 * q + 1]) | (pack_e2m1x2(p[8 * q + 2], p[8 * q + 3]) << 8) |
+                         (pack_e2m1x2(p[8 * q + 4], p[8 * q + 5]) << 16) |
+                         (pack_e2m1x2(p[8 * q + 6], p[8 * q + 7]) << 24);
     }
     return c;
 }
 
-template <int EPT>
-__device__ __forceinline__ void store_codes(uint8_t* p, const MxChunk<EPT>& c) {
-    if constexpr (EPT == 16) {
-        asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(c.codes[0]), "r"(c.codes[1]),
-                     "r"(c.codes[2]), "r"(c.codes[3]) : "memory");
+template <int W>
+__device__ __forceinline__ void store_words(uint8_t* p, const uint32_t (&w)[W]) {
+    if constexpr (W == 4) {
+        asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                     "r"(w[3]) : "memory");
+    } else if constexpr (W == 2) {
+        asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(w[0]), "r"(w[1]) : "memory");
     } else {
-        asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(c.codes[0]), "r"(c.codes[1])
-                     : "memory");
+        asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(w[0]) : "memory");
     }
 }
 
@@ -99,13 +160,21 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-// SwiGLU + MXFP8. Item v = r * nv + c covers act[r, c*EPT .. c*EPT + EPT).
-template <int EPT, int NT>
-__global__ void __launch_bounds__(NT) swiglu_mxfp8_kernel(const uint8_t* __restrict__ gate_up,
-                                                          uint8_t* __restrict__ codes,
-                                                          uint8_t* __restrict__ scales, uint32_t total,
-                                                          DivU32 nv, uint32_t I) {
+// Byte offset of value column col of a row in the code buffer.
+template <int F>
+__device__ __forceinline__ uint64_t code_offset(uint64_t row, uint32_t n, uint32_t col) {
+    return (row * n + col) * FmtInfo<F>::kBits / 8;
+}
+
+// SwiGLU + block quantization. Item v = r * nv + c covers
+// act[r, c*EPT .. c*EPT + EPT).
+template <int F, int EPT, int NT>
+__global__ void __launch_bounds__(NT) swiglu_q_kernel(const uint8_t* __restrict__ gate_up,
+                                                      uint8_t* __restrict__ codes,
+                                                      uint8_t* __restrict__ scales, uint32_t total,
+                                                      DivU32 nv, uint32_t I, float g) {
     constexpr int VB = 2 * EPT;   // bytes of EPT bfloat16 inputs
+    constexpr int kLanes = FmtInfo<F>::kBlock / EPT;
     pdl_wait_and_release();
     const uint32_t stride = gridDim.x * NT;
     // the loop runs the same number of times on every lane of a warp (lanes
@@ -120,12 +189,12 @@ __global__ void __launch_bounds__(NT) swiglu_mxfp8_kernel(const uint8_t* __restr
             r = nv.div(v);
             c = v - r * nv.d;
             const uint8_t* src = gate_up + uint64_t(r) * (4ull * I) + uint64_t(c) * VB;
-            Bits<VB> g, u;
-            ld_stream(g, src);
-            ld_stream(u, src + 2ull * I);
+            Bits<VB> gb, ub;
+            ld_stream(gb, src);
+            ld_stream(ub, src + 2ull * I);
             float gf[EPT], uf[EPT];
-            unpack<EPT>(g, gf);
-            unpack<EPT>(u, uf);
+            unpack<EPT>(gb, gf);
+            unpack<EPT>(ub, uf);
 #pragma unroll
             for (int i = 0; i < EPT; i += 2) {
                 // the bfloat16 value moe_swiglu would store
@@ -137,24 +206,26 @@ __global__ void __launch_bounds__(NT) swiglu_mxfp8_kernel(const uint8_t* __restr
 #pragma unroll
             for (int i = 0; i < EPT; ++i) a[i] = 0.0f;
         }
-        const MxChunk<EPT> q = quantize_chunk<EPT>(a, valid);
+        const QChunk<F, EPT> q = quantize_chunk<F, EPT>(a, valid, g);
         if (valid) {
-            store_codes<EPT>(codes + uint64_t(r) * I + uint64_t(c) * EPT, q);
-            if (c % (32 / EPT) == 0) scales[uint64_t(r) * (I / 32) + c / (32 / EPT)] = uint8_t(q.x + 127);
+            store_words(codes + code_offset<F>(r, I, c * EPT), q.codes);
+            if (c % kLanes == 0)
+                scales[uint64_t(r) * (I / FmtInfo<F>::kBlock) + c / kLanes] = uint8_t(q.scale);
         }
     }
 }
 
-// Expand + MXFP8: item v = t * nv + c covers x[t, c*EPT .. +EPT), quantized
-// once and stored to the token's k rows inv_perm[t*k + j] < rows.
-template <int EPT, int NT>
-__global__ void __launch_bounds__(NT) expand_mxfp8_kernel(const uint8_t* __restrict__ x,
-                                                          uint8_t* __restrict__ codes,
-                                                          uint8_t* __restrict__ scales,
-                                                          const int32_t* __restrict__ inv_perm, int k,
-                                                          uint32_t rows, uint32_t total, DivU32 nv,
-                                                          uint32_t H) {
+// Expand + block quantization: item v = t * nv + c covers x[t, c*EPT .. +EPT),
+// quantized once and stored to the token's k rows inv_perm[t*k + j] < rows.
+template <int F, int EPT, int NT>
+__global__ void __launch_bounds__(NT) expand_q_kernel(const uint8_t* __restrict__ x,
+                                                      uint8_t* __restrict__ codes,
+                                                      uint8_t* __restrict__ scales,
+                                                      const int32_t* __restrict__ inv_perm, int k,
+                                                      uint32_t rows, uint32_t total, DivU32 nv,
+                                                      uint32_t H, float g) {
     constexpr int VB = 2 * EPT;
+    constexpr int kLanes = FmtInfo<F>::kBlock / EPT;
     pdl_wait_and_release();
     const uint32_t stride = gridDim.x * NT;
     const uint32_t first = blockIdx.x * NT + (threadIdx.x & ~31u);
@@ -173,15 +244,15 @@ __global__ void __launch_bounds__(NT) expand_mxfp8_kernel(const uint8_t* __restr
 #pragma unroll
             for (int i = 0; i < EPT; ++i) a[i] = 0.0f;
         }
-        const MxChunk<EPT> q = quantize_chunk<EPT>(a, valid);
+        const QChunk<F, EPT> q = quantize_chunk<F, EPT>(a, valid, g);
         if (valid) {
-            const bool scale_lane = c % (32 / EPT) == 0;
+            const bool scale_lane = c % kLanes == 0;
             const int32_t* ip = inv_perm + uint64_t(t) * k;
             for (int j = 0; j < k; ++j) {
                 const uint32_t p = uint32_t(__ldg(ip + j));
                 if (p >= rows) continue;
-                store_codes<EPT>(codes + uint64_t(p) * H + uint64_t(c) * EPT, q);
-                if (scale_lane) scales[uint64_t(p) * (H / 32) + c / (32 / EPT)] = uint8_t(q.x + 127);
+                store_words(codes + code_offset<F>(p, H, c * EPT), q.codes);
+                if (scale_lane) scales[uint64_t(p) * (H / FmtInfo<F>::kBlock) + c / kLanes] = uint8_t(q.scale);
             }
         }
     }
@@ -189,12 +260,10 @@ __global__ void __launch_bounds__(NT) expand_mxfp8_kernel(const uint8_t* __restr
 
 constexpr int kNt = 256;
 
-// 16 values per thread when the bfloat16 input rows allow 32-byte loads,
-// else 8 (16-byte loads).
-template <int EPT>
+template <int F, int EPT>
 cudaError_t launch_swiglu_q(const uint16_t* gate_up, int64_t rows, int I, uint8_t* codes,
-                            uint8_t* scales, int num_sms, cudaStream_t stream) {
-    auto kernel = swiglu_mxfp8_kernel<EPT, kNt>;
+                            uint8_t* scales, float g, int num_sms, cudaStream_t stream) {
+    auto kernel = swiglu_q_kernel<F, EPT, kNt>;
     static const int occ = resident_blocks(kernel, kNt);
     const uint32_t nv = uint32_t(I / EPT);
     const int64_t per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / nv));
@@ -204,18 +273,19 @@ cudaError_t launch_swiglu_q(const uint16_t* gate_up, int64_t rows, int I, uint8_
         const int grid = grid_for(occ, total, uint64_t(kNt), num_sms);
         const cudaError_t err = launch_pdl(
             kernel, dim3(grid), dim3(kNt), 0, stream,
-            reinterpret_cast<const uint8_t*>(gate_up + r0 * 2 * int64_t(I)), codes + r0 * int64_t(I),
-            scales + r0 * int64_t(I / 32), total, DivU32::make(nv), uint32_t(I));
+            reinterpret_cast<const uint8_t*>(gate_up + r0 * 2 * int64_t(I)),
+            codes + r0 * int64_t(I) * FmtInfo<F>::kBits / 8, scales + r0 * int64_t(I / FmtInfo<F>::kBlock),
+            total, DivU32::make(nv), uint32_t(I), g);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
 }
 
-template <int EPT>
+template <int F, int EPT>
 cudaError_t launch_expand_q(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
-                            int64_t rows, uint8_t* codes, uint8_t* scales, int num_sms,
+                            int64_t rows, uint8_t* codes, uint8_t* scales, float g, int num_sms,
                             cudaStream_t stream) {
-    auto kernel = expand_mxfp8_kernel<EPT, kNt>;
+    auto kernel = expand_q_kernel<F, EPT, kNt>;
     static const int occ = resident_blocks(kernel, kNt);
     const uint32_t nv = uint32_t(H / EPT);
     const int64_t per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / nv));
@@ -225,27 +295,56 @@ cudaError_t launch_expand_q(const uint16_t* x, int64_t T, int H, int k, const in
         const int grid = grid_for(occ, total, uint64_t(kNt), num_sms);
         const cudaError_t err = launch_pdl(
             kernel, dim3(grid), dim3(kNt), 0, stream, reinterpret_cast<const uint8_t*>(x + t0 * int64_t(H)),
-            codes, scales, inv_perm + t0 * k, k, uint32_t(rows), total, DivU32::make(nv), uint32_t(H));
+            codes, scales, inv_perm + t0 * k, k, uint32_t(rows), total, DivU32::make(nv), uint32_t(H), g);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
+}
+
+// 16 values per thread when the bfloat16 input rows allow 32-byte loads and
+// the code buffer the matching store, else 8 (16-byte loads).
+template <int F>
+cudaError_t swiglu_q(const uint16_t* gate_up, int64_t rows, int I, uint8_t* codes, uint8_t* scales, float g,
+                     int num_sms, cudaStream_t stream) {
+    constexpr uint32_t kStore16 = 16 * FmtInfo<F>::kBits / 8;
+    if (can_use_32b(uint64_t(I) * 2, {gate_up}) && reinterpret_cast<uintptr_t>(codes) % kStore16 == 0)
+        return launch_swiglu_q<F, 16>(gate_up, rows, I, codes, scales, g, num_sms, stream);
+    return launch_swiglu_q<F, 8>(gate_up, rows, I, codes, scales, g, num_sms, stream);
+}
+
+template <int F>
+cudaError_t expand_q(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm, int64_t rows,
+                     uint8_t* codes, uint8_t* scales, float g, int num_sms, cudaStream_t stream) {
+    constexpr uint32_t kStore16 = 16 * FmtInfo<F>::kBits / 8;
+    if (can_use_32b(uint64_t(H) * 2, {x}) && reinterpret_cast<uintptr_t>(codes) % kStore16 == 0)
+        return launch_expand_q<F, 16>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream);
+    return launch_expand_q<F, 8>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_swiglu_mxfp8(const uint16_t* gate_up, int64_t rows, int I, uint8_t* codes,
                                 uint8_t* scales, int num_sms, cudaStream_t stream) {
-    if (can_use_32b(uint64_t(I) * 2, {gate_up}) && reinterpret_cast<uintptr_t>(codes) % 16 == 0)
-        return launch_swiglu_q<16>(gate_up, rows, I, codes, scales, num_sms, stream);
-    return launch_swiglu_q<8>(gate_up, rows, I, codes, scales, num_sms, stream);
+    return swiglu_q<kMxfp8>(gate_up, rows, I, codes, scales, 0.0f, num_sms, stream);
 }
 
 cudaError_t launch_expand_mxfp8(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
                                 int64_t rows, uint8_t* codes, uint8_t* scales, int num_sms,
                                 cudaStream_t stream) {
-    if (can_use_32b(uint64_t(H) * 2, {x}) && reinterpret_cast<uintptr_t>(codes) % 16 == 0)
-        return launch_expand_q<16>(x, T, H, k, inv_perm, rows, codes, scales, num_sms, stream);
-    return launch_expand_q<8>(x, T, H, k, inv_perm, rows, codes, scales, num_sms, stream);
+    return expand_q<kMxfp8>(x, T, H, k, inv_perm, rows, codes, scales, 0.0f, num_sms, stream);
+}
+
+cudaError_t launch_swiglu_fp4(const uint16_t* gate_up, int64_t rows, int I, bool nvfp4, float g,
+                              uint8_t* codes, uint8_t* scales, int num_sms, cudaStream_t stream) {
+    return nvfp4 ? swiglu_q<kNvfp4>(gate_up, rows, I, codes, scales, g, num_sms, stream)
+                 : swiglu_q<kMxfp4>(gate_up, rows, I, codes, scales, 0.0f, num_sms, stream);
+}
+
+cudaError_t launch_expand_fp4(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
+                              int64_t rows, bool nvfp4, float g, uint8_t* codes, uint8_t* scales,
+                              int num_sms, cudaStream_t stream) {
+    return nvfp4 ? expand_q<kNvfp4>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream)
+                 : expand_q<kMxfp4>(x, T, H, k, inv_perm, rows, codes, scales, 0.0f, num_sms, stream);
 }
 
 }  // namespace moe

@@ -210,6 +210,30 @@ def test_mxfp8_rules(lib, nogpu):
     assert lib.moe_expand_mxfp8(A[0], 16, 256, 2, A[1], 32, A[0], A[3], None) == INVALID   # codes over x
 
 
+def test_fp4_rules(lib, nogpu):
+    NV, MX = 0, 1
+    sw = lambda *a: lib.moe_swiglu_fp4(*a)
+    assert sw(A[0], 16, 64, 2, 1.0, A[1], A[2], None) == INVALID                  # unknown format
+    assert sw(A[0], 16, 64, NV, 0.0, A[1], A[2], None) == INVALID                 # NVFP4 scale must be > 0
+    assert sw(A[0], 16, 64, NV, -1.0, A[1], A[2], None) == INVALID
+    assert sw(A[0], 16, 64, NV, float("inf"), A[1], A[2], None) == INVALID
+    assert sw(A[0], 16, 64, NV, float("nan"), A[1], A[2], None) == INVALID
+    assert sw(A[0], 16, 48, MX, 1.0, A[1], A[2], None) == MISALIGNED              # I % 32 for MXFP4
+    assert sw(A[0], 16, 40, NV, 1.0, A[1], A[2], None) == MISALIGNED              # I % 16 for NVFP4
+    assert sw(A[0], 16, 64, MX, 0.0, A[1] + 8, A[2], None) == MISALIGNED          # codes alignment
+    assert sw(A[0], 16, 64, MX, 0.0, 0, A[2], None) == INVALID
+    assert sw(A[0], 16, 64, NV, 1.0, A[0] + 64, A[2], None) == INVALID            # codes over gate_up
+    assert sw(0, 0, 64, NV, 1.0, 0, 0, None) == OK                                # nothing to do
+    ex = lambda *a: lib.moe_expand_fp4(*a)
+    assert ex(A[0], 16, 264, 2, A[1], 32, MX, 0.0, A[2], A[3], None) == MISALIGNED   # H % 32
+    assert ex(A[0], 16, 264, 2, A[1], 32, NV, 1.0, A[2], A[3], None) == MISALIGNED   # H % 16
+    assert ex(A[0], 16, 256, 2, A[1], 32, 5, 1.0, A[2], A[3], None) == INVALID
+    assert ex(A[0], 16, 256, 2, A[1], -1, NV, 1.0, A[2], A[3], None) == INVALID
+    assert ex(A[0], 16, 256, 2, A[1], 32, NV, 1.0, A[2], 0, None) == INVALID
+    assert ex(A[0], 16, 256, 2, A[1], 32, NV, 1.0, A[0], A[3], None) == INVALID      # codes over x
+    assert ex(A[0], 16, 256, 17, A[1], 32, NV, 1.0, A[2], A[3], None) == UNSUPPORTED  # k > 16
+
+
 def test_qk_rmsnorm_rules(lib, nogpu):
     f = lambda *a: lib.moe_qk_rmsnorm(*a)
     import ctypes as C
