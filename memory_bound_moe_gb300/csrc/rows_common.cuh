@@ -76,6 +76,11 @@ inline uint64_t l2_bytes() {
 
 // Work items per launch stay below 2^31 so 32-bit grid-stride indices never
 // wrap; larger jobs are split into several launches over row ranges.
-constexpr uint64_t kMaxItemsPerLaunch = uint64_t(1) << 30;
+// (A build may lower it, MOE_MAX_ITEMS_PER_LAUNCH, to test the splitting on
+// small inputs.)
+#ifndef MOE_MAX_ITEMS_PER_LAUNCH
+#define MOE_MAX_ITEMS_PER_LAUNCH (uint64_t(1) << 30)
+#endif
+constexpr uint64_t kMaxItemsPerLaunch = MOE_MAX_ITEMS_PER_LAUNCH;
 
 }  // namespace moe
