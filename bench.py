@@ -775,6 +775,14 @@ def main():
     decode = decode_latency(dev, reps=args.extra_reps or 2000) if more else None
     extras = extras_measurement(dev, reps=args.extra_reps or 240) if more else None
 
+    # the dominant kernel measured alone (extras: back-to-back launches over
+    # rotating input/output sets), beside the in-step figure above, which
+    # also carries the previous kernel's write-backs
+    alone = (extras or {}).get(f"{dominant}_bf16")
+    if alone is not None:
+        roofline["alone_GBps"] = alone["GBps"]
+        roofline["alone_frac"] = alone["frac"]
+
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         cpu = cpu_baseline(w, inputs, args.cpu_budget)
