@@ -38,7 +38,9 @@
  *   - A zero-sized batch (T = 0 or rows = 0) is valid; pointers of empty
  *     arrays may then be NULL.
  *   - The functions are thread-safe and keep no mutable global state apart
- *     from a per-device cache of the SM count.
+ *     from a per-device cache of the SM count. The one exception is
+ *     moe_route_static, whose calls share one static scratch array and so
+ *     must not overlap on the GPU (see its comment below).
  *
  * Page citations name the page title and section; the pages themselves
  * state no formulas, so the definitions below are the plain readings
@@ -167,9 +169,12 @@ moe_status_t moe_route_expand(const float* logits, int64_t T, int E, int k, int 
  *     process exits. Sizes whose workspace (moe_route_workspace_size) exceeds
  *     it are rejected with MOE_ERR_WORKSPACE before anything is launched; no
  *     size accepted by moe_route currently needs more than 128 KiB.
- *   - The first call on a device (while that device is current) looks up the
- *     array's device address and caches it; make that first call before any
- *     stream capture on that device.
+ *   - Every call looks up the array's device address in the current CUDA
+ *     context (cudaGetSymbolAddress, which allocates nothing), so the
+ *     address stays right after cudaDeviceReset or with another context
+ *     current. The first call in a context may load the library's device
+ *     code into it: make that first call before any stream capture on that
+ *     device.
  *   - All calls share the one array and it keeps whatever the last call left
  *     there. Nothing in it has to start at zero: each call writes every entry
  *     it later reads. Calls that can overlap on the GPU (different streams

@@ -5,42 +5,28 @@
 // The array is a module global: every device that loads this library holds
 // MOE_ROUTE_STATIC_SCRATCH_BYTES of it until the process exits. Host code
 // must not pass the array's name to a kernel (on the host it is only a
-// stand-in symbol); its device address is looked up once per device with
-// cudaGetSymbolAddress while that device is current, cached, and handed to
-// the ordinary routing launch as its workspace pointer.
+// stand-in symbol); its device address is looked up with
+// cudaGetSymbolAddress, while the caller's device is current, on every call
+// and handed to the ordinary routing launch as its workspace pointer. The
+// lookup allocates nothing. It is not cached: the address belongs to the
+// CUDA context that loaded the module, and after cudaDeviceReset (or with
+// another context current on the same device) the module is loaded again
+// and the array may sit elsewhere, so a cached address could go stale.
 #include "moe_glue.h"
 
 #include <cuda_runtime.h>
-
-#include <atomic>
-#include <mutex>
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_route_scratch[MOE_ROUTE_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
-std::mutex g_setup_mutex;
-
-// Device address of g_route_scratch on the current device; the first call
-// on a device does the lookup.
+// Device address of g_route_scratch in the current context. The first lookup
+// in a context may load the library's device code into it.
 cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&p, g_route_scratch);
     if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
-        std::lock_guard<std::mutex> lock(g_setup_mutex);
-        p = g_scratch_addr[dev].load(std::memory_order_acquire);
-        if (p == nullptr) {
-            err = cudaGetSymbolAddress(&p, g_route_scratch);
-            if (err != cudaSuccess) return err;
-            if (p == nullptr) return cudaErrorInvalidSymbol;
-            g_scratch_addr[dev].store(p, std::memory_order_release);
-        }
-    }
+    if (p == nullptr) return cudaErrorInvalidSymbol;
     *out = p;
     return cudaSuccess;
 }
