@@ -17,3 +17,20 @@ def oracle_mod():
     from oracle import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def oracle_act(oracle_mod):
+    """Memoised (gate_up, oracle act) of a named workload, as bfloat16 bit
+    patterns: the oracle's SwiGLU of the full batch is computed once per
+    session and shared by every test that compares against it."""
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            from memory_bound_moe_gb300.workloads import WORKLOADS, as_u16, generate
+            gu = as_u16(generate(WORKLOADS[name], seed=0, parts=("gate_up",))["gate_up"])
+            cache[name] = (gu, oracle_mod.swiglu(gu))
+        return cache[name]
+
+    return get

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import check_exact
+from helpers import check_exact, check_quant_where_inputs_agree
 
 pytestmark = pytest.mark.gpu
 
@@ -131,7 +131,12 @@ def test_swiglu_fp4_against_oracle(dev, oracle_mod, fmt, g, rows, I, wide):
     check_exact(s, es, f"{fmt} scales rows={rows} I={I}")
     check_exact(c, ec, f"{fmt} codes rows={rows} I={I}")
     # near: against the oracle's act, dequantized values within one E2M1 unit
-    rc, rs = _quant(O, fmt, g, O.swiglu(gu))
+    ref_act = O.swiglu(gu)
+    rc, rs = _quant(O, fmt, g, ref_act)
+    # independent: the oracle's quantization of its own act, wherever the
+    # bfloat16 act and the block scale agree
+    check_quant_where_inputs_agree(c, s, rc, rs, u16(act), ref_act, 16 if fmt == "nvfp4" else 32, True,
+                                   f"{fmt} rows={rows} I={I}")
     if fmt == "nvfp4":
         deq, ref = O.dequant_nvfp4(c, s, g), O.dequant_nvfp4(rc, rs, g)
         unit = np.repeat(np.maximum(O.e4m3_decode(s), O.e4m3_decode(rs)), 16, axis=1) / g
@@ -142,33 +147,41 @@ def test_swiglu_fp4_against_oracle(dev, oracle_mod, fmt, g, rows, I, wide):
     assert (c == rc).mean() >= 0.99, fmt
 
 
-def test_fp4_prefill_sampled(dev, oracle_mod):
-    """The prefill shapes: SwiGLU 16384 x 14336 outputs and expand of 8192 x
-    4096 rows, NVFP4 with a calibrated tensor scale; sampled row blocks
-    against the oracle's quantization of the bfloat16 outputs."""
+def test_fp4_prefill_full(dev, oracle_mod, oracle_act):
+    """The prefill shapes in full: SwiGLU 16384 x 14336 outputs (NVFP4 with a
+    calibrated tensor scale) and expand of 8192 x 4096 token rows (MXFP4).
+    SwiGLU: bit-exact against the oracle's quantization of the GPU's bfloat16
+    act, and against the oracle's quantization of its own act wherever the
+    two acts and the block scale agree; expand: bit-exact."""
     from memory_bound_moe_gb300 import moe_expand_fp4, moe_swiglu, moe_swiglu_fp4
     from memory_bound_moe_gb300.workloads import WORKLOADS, as_u16, generate
     O = oracle_mod
     w = WORKLOADS["prefill"]
-    gu = as_u16(generate(w, seed=0, parts=("gate_up",))["gate_up"])
+    gu, ref_act = oracle_act("prefill")
     gd = bf16_dev(gu, dev)
     act = moe_swiglu(gd)
     g = 448.0 * 6.0 / float(act.float().abs().max())
     codes, scales = moe_swiglu_fp4(gd, "nvfp4", g)
     torch.cuda.synchronize()
+    del gd
     a16, c, s = u16(act), codes.cpu().numpy(), scales.cpu().numpy()
-    for lo, hi in [(0, 64), (8192 - 32, 8192 + 32), (16384 - 64, 16384)]:
+    del act, codes, scales
+    rows = a16.shape[0]
+    for lo in range(0, rows, 1024):
+        hi = min(rows, lo + 1024)
         ec, es = O.quant_nvfp4(a16[lo:hi], g)
         check_exact(s[lo:hi], es, f"prefill swiglu scales [{lo},{hi})")
         check_exact(c[lo:hi], ec, f"prefill swiglu codes [{lo},{hi})")
+        rc, rs = O.quant_nvfp4(ref_act[lo:hi], g)
+        check_quant_where_inputs_agree(c[lo:hi], s[lo:hi], rc, rs, a16[lo:hi], ref_act[lo:hi], 16, True,
+                                       f"prefill swiglu [{lo},{hi})")
     x = as_u16(generate(w, seed=0, parts=("x",))["x"])
     T, k = w.T, w.k
     inv = torch.arange(T * k, dtype=torch.int32, device=dev)        # identity rows: row t*k+j = token t
     codes, scales = moe_expand_fp4(bf16_dev(x, dev), inv, k, "mxfp4")
     torch.cuda.synchronize()
     c, s = codes.cpu().numpy(), scales.cpu().numpy()
-    for lo, hi in [(0, 32), (4096, 4128), (8192 - 32, 8192)]:
-        ec, es = O.quant_mxfp4(x[lo:hi])
-        for j in range(k):
-            check_exact(s[lo * k + j:hi * k:k], es, f"prefill expand scales [{lo},{hi}) j={j}")
-            check_exact(c[lo * k + j:hi * k:k], ec, f"prefill expand codes [{lo},{hi}) j={j}")
+    ec, es = O.quant_mxfp4(x)
+    for j in range(k):
+        check_exact(s[j::k], es, f"prefill expand scales j={j}")
+        check_exact(c[j::k], ec, f"prefill expand codes j={j}")

@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import check_exact
+from helpers import check_exact, check_quant_where_inputs_agree
 
 pytestmark = pytest.mark.gpu
 
@@ -99,8 +99,8 @@ def test_expand_mxfp8_into_padded_local_rows(dev, oracle_mod):
     check_exact(scales.cpu().numpy(), ref_s, "padded scales")
 
 
-def _check_swiglu_q(O, codes, scales, gu, what):
-    ref_c, ref_s = O.quant_mxfp8(O.swiglu(gu))
+def _check_swiglu_q(O, codes, scales, gu, what, ref_act=None):
+    ref_c, ref_s = O.quant_mxfp8(O.swiglu(gu) if ref_act is None else ref_act)
     same_scale = scales == ref_s
     assert same_scale.mean() >= 1 - 1e-4, (what, float(same_scale.mean()))
     deq = O.dequant_mxfp8(codes, scales)
@@ -111,12 +111,13 @@ def _check_swiglu_q(O, codes, scales, gu, what):
     bad = (np.abs(deq - ref) > bound) & blk
     assert not bad.any(), (what, np.argwhere(bad)[:5])
     assert (codes == ref_c)[blk].mean() >= 0.999, what
+    return ref_c, ref_s
 
 
 @pytest.mark.parametrize("rows,I", [(128, 128), (32768, 768), (128, 2048), (4092, 2880), (7, 32)])
 @pytest.mark.parametrize("wide", [True, False])
 def test_swiglu_mxfp8_against_oracle(dev, oracle_mod, rows, I, wide):
-    from memory_bound_moe_gb300 import moe_swiglu_mxfp8
+    from memory_bound_moe_gb300 import moe_swiglu, moe_swiglu_mxfp8
     O = oracle_mod
     rng = np.random.default_rng(rows + I)
     gu = O.bf16_round(rng.standard_normal((rows, 2 * I)) * 2)
@@ -124,21 +125,32 @@ def test_swiglu_mxfp8_against_oracle(dev, oracle_mod, rows, I, wide):
     if not wide:
         gd = _offset16(gd)
     codes, scales = moe_swiglu_mxfp8(gd)
+    act = u16(moe_swiglu(gd))
     torch.cuda.synchronize()
-    _check_swiglu_q(O, codes.cpu().numpy(), scales.cpu().numpy(), gu, f"rows={rows} I={I}")
-
-
-def test_swiglu_mxfp8_prefill_sampled(dev, oracle_mod):
-    """The prefill shape (16384 x 14336 outputs): sampled row blocks."""
-    from memory_bound_moe_gb300 import moe_swiglu_mxfp8
-    from memory_bound_moe_gb300.workloads import WORKLOADS, as_u16, generate
-    O = oracle_mod
-    w = WORKLOADS["prefill"]
-    gu = as_u16(generate(w, seed=0, parts=("gate_up",))["gate_up"])
-    codes, scales = moe_swiglu_mxfp8(bf16_dev(gu, dev))
     c, s = codes.cpu().numpy(), scales.cpu().numpy()
-    for a, b in [(0, 128), (8192 - 64, 8192 + 64), (16384 - 128, 16384)]:
-        _check_swiglu_q(O, c[a:b], s[a:b], gu[a:b], f"prefill rows {a}:{b}")
+    ref_act = O.swiglu(gu)
+    ref_c, ref_s = _check_swiglu_q(O, c, s, gu, f"rows={rows} I={I}", ref_act)
+    check_quant_where_inputs_agree(c, s, ref_c, ref_s, act, ref_act, 32, False, f"rows={rows} I={I}")
+
+
+def test_swiglu_mxfp8_prefill_full(dev, oracle_mod, oracle_act):
+    """The prefill shape (16384 x 14336 outputs), every block, compared in
+    row chunks against the oracle's quantization of its own act."""
+    from memory_bound_moe_gb300 import moe_swiglu, moe_swiglu_mxfp8
+    O = oracle_mod
+    gu, ref_act = oracle_act("prefill")
+    gd = bf16_dev(gu, dev)
+    codes, scales = moe_swiglu_mxfp8(gd)
+    act = u16(moe_swiglu(gd))
+    torch.cuda.synchronize()
+    del gd
+    c, s = codes.cpu().numpy(), scales.cpu().numpy()
+    rows = gu.shape[0]
+    for a in range(0, rows, 1024):
+        b = min(rows, a + 1024)
+        ref_c, ref_s = _check_swiglu_q(O, c[a:b], s[a:b], None, f"prefill rows {a}:{b}", ref_act[a:b])
+        check_quant_where_inputs_agree(c[a:b], s[a:b], ref_c, ref_s, act[a:b], ref_act[a:b], 32, False,
+                                       f"prefill rows {a}:{b}")
 
 
 def test_swiglu_mxfp8_dequantizes_to_swiglu(dev, oracle_mod):

@@ -94,20 +94,16 @@ def test_expand_workload(dev, O, name):
 
 
 @pytest.mark.parametrize("name", CONFIGS)
-def test_swiglu_workload(dev, O, name):
+def test_swiglu_workload(dev, oracle_act, name):
+    """Every element of every workload's act, prefill's 16384 x 14336
+    included (compared in chunks)."""
     from memory_bound_moe_gb300 import moe_swiglu
-    w, inp = workload_inputs(name)
-    gu = u16(inp["gate_up"])
+    gu, ref = oracle_act(name)
     act = u16(moe_swiglu(bf16_dev(gu, dev)))
-    if name == "prefill":
-        # 16384 x 14336 outputs: check sampled row blocks at the start, middle
-        # and end (the kernel flattens rows, so blocks cross row boundaries).
-        S = gu.shape[0]
-        blocks = [(0, 256), (S // 2 - 128, S // 2 + 128), (S - 256, S)]
-        for a, b in blocks:
-            check_bf16_close(act[a:b], O.swiglu(gu[a:b]), f"{name} act rows {a}:{b}")
-    else:
-        check_bf16_close(act, O.swiglu(gu), f"{name} act")
+    stats = check_bf16_close(act, ref, f"{name} act")
+    # one float32 evaluation rounded once: nearly every element is the
+    # correctly rounded value
+    assert stats["exact_frac"] > 0.999, stats
 
 
 @pytest.mark.parametrize("name", CONFIGS)
@@ -127,24 +123,27 @@ def test_combine_workload(dev, O, name):
 
 
 @pytest.mark.parametrize("name", CONFIGS)
-def test_whole_path_workload(dev, O, name):
+def test_whole_path_workload(dev, O, oracle_act, name):
     """route -> expand -> SwiGLU -> combine on the GPU, each stage fed by the
-    GPU's previous stage, against the oracle's path on the same inputs."""
+    GPU's previous stage, against the oracle's path on the same inputs; every
+    output compared in full."""
     from memory_bound_moe_gb300 import moe_combine, moe_expand, moe_route, moe_swiglu
     w, inp = workload_inputs(name)
     logits = inp["logits"].to(dev)
     x = inp["x"].to(dev)
     r = moe_route(logits, w.k, w.renorm)
     ex = moe_expand(x, r.inv_perm, w.k)
-    if name != "prefill":
-        act = moe_swiglu(inp["gate_up"].to(dev))
+    act = moe_swiglu(inp["gate_up"].to(dev))
     out = moe_combine(inp["expert_out"].to(dev), r.topk_weights, r.inv_perm)
     torch.cuda.synchronize()
     ref = O.route(inp["logits"].numpy(), w.k, w.renorm)
     assert_route_equal({f: getattr(r, f).cpu().numpy() for f in r._fields}, ref, name)
     check_exact(u16(ex), O.expand(u16(inp["x"]), w.k, ref["perm"]), f"{name} expanded_x")
-    if name != "prefill":
-        check_bf16_close(u16(act), O.swiglu(u16(inp["gate_up"])), f"{name} act")
+    del ex
+    gu, ref_act = oracle_act(name)
+    assert np.array_equal(gu, u16(inp["gate_up"]))
+    check_bf16_close(u16(act), ref_act, f"{name} act")
+    del act
     check_bf16_close(u16(out), O.combine(u16(inp["expert_out"]), ref["topk_weights"],
                                          ref["inv_perm"]), f"{name} out")
 
