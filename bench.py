@@ -3,24 +3,28 @@
 
 One step = one pass of the whole path over one batch of synthetic input:
 moe_route (softmax, top-k, histogram/scan, permutation) -> moe_expand ->
-moe_swiglu -> moe_combine, all through the C ABI. The workload is the
-T=4096, H=2048, E=128, top-8 (renormalised), I=768 layer. Inputs are seeded
-and synthetic (memory_bound_moe_gb300.workloads); the expert GEMMs are not
-part of the path, so their outputs (gate_up, expert_out) are inputs here.
+moe_swiglu -> moe_combine, all through the C ABI. The headline workload is
+the largest layer, the prefill batch: T=8192 tokens, H=4096, E=8 experts,
+top-2 (renormalised), I=14336 (1.81 GB of algorithmic traffic per step).
+Inputs are seeded and synthetic (memory_bound_moe_gb300.workloads); the
+expert GEMMs are not part of the path, so their outputs (gate_up,
+expert_out) are inputs here.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload prefill|mid|skewed|decode|tiny]
 
 Prints one JSON line (rank 0). Timing: CUDA events on the launching stream
-around K back-to-back steps (one step streams ~450 MB, inputs 252 MB, through
-the 129 MB L2, so inputs come from HBM every step; no flush writes, whose
-dirty lines would be written back inside the next step), plus events between
-the four calls for the per-kernel split; device-resident `value` and an
-end-to-end `e2e` measured through the
-public Python binding with pinned host buffers and the host<->device copies
-inside the timed region. With N > 1 (torchrun) every rank runs its own
-replica on its own batch (weak scaling, no collective on the data path);
-the step time is the max over ranks. `--impl reference` times the CPU oracle
-(plain C, one thread) on a bounded sample of the same workload instead.
+around K back-to-back steps (one prefill step streams 1.81 GB, inputs
+1.14 GB, through the 129 MB L2, so inputs come from HBM every step; no flush
+writes, whose dirty lines would be written back inside the next step), plus
+events between the four calls for the per-kernel split; device-resident
+`value` and an end-to-end `e2e` measured through the public Python binding
+with pinned host buffers and the host<->device copies inside the timed
+region. The other workloads (mid, skewed, decode, tiny) are timed the same
+way and reported under `workloads`. With N > 1 (torchrun) every rank runs
+its own replica on its own batch (weak scaling, no collective on the data
+path); the step time is the max over ranks. `--impl reference` times the CPU
+oracle (plain C) on the host cores on bounded samples of the same workload.
 """
 from __future__ import annotations
 
@@ -38,7 +42,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-WORKLOAD = "mid"
+WORKLOAD = "prefill"
+SIDE_WORKLOADS = ("mid", "skewed", "decode", "tiny")
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 KERNELS = ("route", "expand", "swiglu", "combine")
@@ -51,7 +56,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=WORKLOAD, help="workload name (default: mid)")
+    ap.add_argument("--workload", default=WORKLOAD, help="workload name (default: prefill)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle CPU work for the cpu_baseline leg (0 = skip)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -400,13 +405,17 @@ def time_e2e(w, inputs, steps, warmup, dev, n_copy_streams=4, chunk_bytes=32 << 
     return ms, h2d, d2h_bytes
 
 
-def decode_latency(dev, reps=2000):
+def decode_latency(dev, reps=2000, layers=16):
     """Latency of one MoE-layer pass on the decode workload (T=16, H=7168,
     E=256, top-8, I=2048): the four calls (route, expand, SwiGLU, combine)
     and the three calls with routing and expansion in one launch
-    (moe_route_expand), each issued back to back through direct C-ABI calls
-    and replayed from a CUDA graph captured once. Per-layer time = elapsed
-    time over `reps` passes / reps."""
+    (moe_route_expand), each issued back to back through direct C-ABI calls,
+    and replayed from CUDA graphs: one graph holding `layers` consecutive
+    layer passes (as a decode step's graph holds every layer of the model),
+    and, for comparison, a graph of a single pass replayed back to back
+    (every replay then starts with a full kernel boundary: programmatic
+    launch overlap does not cross graph launches). Per-layer time = elapsed
+    time / layer passes."""
     import torch
     import memory_bound_moe_gb300 as moe
     from memory_bound_moe_gb300.workloads import WORKLOADS, generate
@@ -442,7 +451,7 @@ def decode_latency(dev, reps=2000):
         st |= lib.moe_combine(p(inp["expert_out"]), T, H, k, p(wts), p(inv), p(out), sp)
         assert st == 0
 
-    def timed(fn):
+    def timed(fn, passes=1, n=reps):
         sp = torch.cuda.current_stream(dev).cuda_stream
         for _ in range(20):
             fn(sp)
@@ -451,13 +460,13 @@ def decode_latency(dev, reps=2000):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
-        for _ in range(reps):
+        for _ in range(n):
             fn(sp)
         b.record()
         torch.cuda.synchronize(dev)
-        return 1e3 * a.elapsed_time(b) / reps
+        return 1e3 * a.elapsed_time(b) / (n * passes)
 
-    def graphed(fn):
+    def graphed(fn, passes):
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(side):
@@ -465,12 +474,17 @@ def decode_latency(dev, reps=2000):
         torch.cuda.synchronize(dev)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            fn(torch.cuda.current_stream(dev).cuda_stream)
+            for _ in range(passes):
+                fn(torch.cuda.current_stream(dev).cuda_stream)
         return lambda sp: g.replay()
 
+    n_graph = max(1, reps // layers)
     res = {"four_calls_stream_us": timed(four), "route_expand_stream_us": timed(three),
-           "four_calls_graph_us": timed(graphed(four)), "route_expand_graph_us": timed(graphed(three)),
-           "workload": w.describe()}
+           "four_calls_graph_us": timed(graphed(four, layers), layers, n_graph),
+           "route_expand_graph_us": timed(graphed(three, layers), layers, n_graph),
+           "four_calls_graph_1layer_us": timed(graphed(four, 1)),
+           "route_expand_graph_1layer_us": timed(graphed(three, 1)),
+           "graph_layers": layers, "workload": w.describe()}
     return {kk: (round(v, 3) if isinstance(v, float) else v) for kk, v in res.items()}
 
 
@@ -589,39 +603,105 @@ def extras_measurement(dev, reps=240, n_sets=3):
 # the CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w, inputs, n_tokens):
-    """The oracle's whole path on the first n_tokens tokens of the batch
-    (their k slots' rows of gate_up / expert_out); returns seconds."""
+def _oracle_batches(w, inputs, n_tokens, parts):
+    """The first n_tokens tokens of the batch cut into `parts` contiguous
+    token ranges, each an independent sub-batch (its logits and x rows and
+    its k slots' rows of gate_up / expert_out) as C-contiguous numpy arrays."""
     import numpy as np
-    from oracle import oracle
     from memory_bound_moe_gb300.workloads import as_u16
     n = max(1, min(n_tokens, w.T))
-    logits = inputs["logits"][:n].numpy()
-    x = as_u16(inputs["x"][:n])
-    gu = as_u16(inputs["gate_up"][: n * w.k])
-    eo = as_u16(inputs["expert_out"][: n * w.k])
+    parts = max(1, min(parts, n))
+    logits = inputs["logits"].numpy()
+    x, gu, eo = as_u16(inputs["x"]), as_u16(inputs["gate_up"]), as_u16(inputs["expert_out"])
+    cuts = [n * i // parts for i in range(parts + 1)]
+    out = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        out.append((np.ascontiguousarray(logits[a:b]), np.ascontiguousarray(x[a:b]),
+                    np.ascontiguousarray(gu[a * w.k:b * w.k]), np.ascontiguousarray(eo[a * w.k:b * w.k])))
+    return n, out
+
+
+def oracle_steps(w, batch):
+    """The oracle's four steps on one sub-batch, each timed on its own;
+    returns {step: seconds}."""
+    from oracle import oracle
+    logits, x, gu, eo = batch
+    t = {}
     t0 = time.perf_counter()
-    oracle.path(np.ascontiguousarray(logits), x, gu, eo, w.k, w.renorm)
-    return time.perf_counter() - t0
+    r = oracle.route(logits, w.k, w.renorm)
+    t1 = time.perf_counter()
+    oracle.expand(x, w.k, r["perm"])
+    t2 = time.perf_counter()
+    oracle.swiglu(gu)
+    t3 = time.perf_counter()
+    oracle.combine(eo, r["topk_weights"], r["inv_perm"])
+    t4 = time.perf_counter()
+    t["route"], t["expand"], t["swiglu"], t["combine"] = t1 - t0, t2 - t1, t3 - t2, t4 - t3
+    return t
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover - non-Linux
+        return os.cpu_count() or 1
+
+
+def oracle_pass(w, batches, threads):
+    """One pass of the oracle over the sub-batches, `threads` at a time
+    (the C oracle runs outside the interpreter lock, so threads run it in
+    parallel). Returns (seconds, summed per-step seconds)."""
+    import concurrent.futures as cf
+    t0 = time.perf_counter()
+    if threads == 1:
+        per = [oracle_steps(w, b) for b in batches]
+    else:
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            per = list(ex.map(lambda b: oracle_steps(w, b), batches))
+    dt = time.perf_counter() - t0
+    return dt, {s: sum(p[s] for p in per) for s in KERNELS}
 
 
 def cpu_baseline(w, inputs, budget_s):
+    """The unchanged oracle on this machine's host cores: single-threaded, then
+    one thread per core over independent token sub-batches, each for about
+    half of `budget_s`. Reports tokens/s for both and the per-step split."""
     from oracle import oracle
     oracle.build()
-    oracle_sample(w, inputs, 8)  # load + warm
-    passes, tokens, spent = 0, 0, 0.0
-    while spent < budget_s and passes < 20:
-        spent += oracle_sample(w, inputs, w.T)
-        tokens += w.T
-        passes += 1
-    return {"value": tokens / spent, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{passes} full pass(es) of the {w.describe()} batch ({tokens} tokens, {spent:.1f} s), "
-                      "single-threaded C oracle in float64"}
+    cores = host_cores()
+    _, warm = _oracle_batches(w, inputs, 16, 1)
+    oracle_steps(w, warm[0])                                   # load + warm
+    probe = oracle_pass(w, _oracle_batches(w, inputs, 256, 1)[1], 1)[0] / min(256, w.T)
+    res = {}
+    for label, threads in (("1core", 1), ("all_cores", cores)):
+        n_tok = int(max(16, min(w.T, budget_s / 2 * threads / max(probe, 1e-9) / 3)))
+        n, batches = _oracle_batches(w, inputs, n_tok, threads)
+        spent, tokens, passes = 0.0, 0, 0
+        steps = {s: 0.0 for s in KERNELS}
+        while passes < 1 or (spent < budget_s / 2 and passes < 20):
+            dt, per = oracle_pass(w, batches, threads)
+            spent += dt
+            tokens += n
+            passes += 1
+            for s in KERNELS:
+                steps[s] += per[s]
+        tot = sum(steps.values())
+        res[label] = {"value": tokens / spent, "threads": threads, "tokens": tokens, "seconds": round(spent, 3),
+                      "step_share": {s: round(steps[s] / tot, 4) for s in KERNELS},
+                      "step_us_per_token": {s: round(1e6 * steps[s] / tokens, 3) for s in KERNELS}}
+    one, allc = res["1core"], res["all_cores"]
+    return {"value": allc["value"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "value_1core": one["value"], "per_step": res,
+            "sample": f"{one['tokens']} tokens on 1 thread and {allc['tokens']} tokens on {cores} threads "
+                      f"(token sub-batches of the {w.describe()} batch, each routed, expanded, activated "
+                      "and combined on its own); plain C oracle in float64, unchanged; per-step split "
+                      "summed over the threads' own step times"}
 
 
 def reference_arm(args, rank, world):
     """The oracle as the reference implementation, timed on host cores on
-    rank 0 only; each step is a bounded sample of the workload."""
+    rank 0 only: each step is one pass over a bounded sample of the workload,
+    cut into one independent token sub-batch per core."""
     if rank != 0:
         return
     from memory_bound_moe_gb300.workloads import WORKLOADS, generate
@@ -629,23 +709,29 @@ def reference_arm(args, rank, world):
     inputs = generate(w, seed=0)
     from oracle import oracle
     oracle.build()
-    t_probe = oracle_sample(w, inputs, 64) / 64           # seconds per token
+    cores = host_cores()
+    _, warm = _oracle_batches(w, inputs, 16, 1)
+    oracle_steps(w, warm[0])
+    t_probe = oracle_pass(w, _oracle_batches(w, inputs, 64, 1)[1], 1)[0] / min(64, w.T)  # s per token, 1 thread
     budget = 90.0                                          # whole run, seconds
-    n = int(max(1, min(w.T, budget / max(1, args.steps + args.warmup) / max(t_probe, 1e-9))))
+    per_step = budget / max(1, args.steps + args.warmup)
+    n_tok = int(max(1, min(w.T, per_step * cores / 2 / max(t_probe, 1e-9))))
+    n, batches = _oracle_batches(w, inputs, n_tok, cores)
     for _ in range(args.warmup):
-        oracle_sample(w, inputs, n)
+        oracle_pass(w, batches, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_sample(w, inputs, n)
+        oracle_pass(w, batches, cores)
     dt = time.perf_counter() - t0
     value = n * args.steps / dt
-    sample = f"first {n} of {w.T} tokens of the {w.describe()} batch per step"
+    sample = (f"first {n} of {w.T} tokens of the {w.describe()} batch per step, as {len(batches)} "
+              f"token sub-batches on {cores} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_dict(w),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -695,15 +781,92 @@ def job_throughput(world: int, tokens_per_rank: int, ms_step_max: float) -> floa
     return world * tokens_per_rank / (ms_step_max * 1e-3)
 
 
+def step_bytes(w) -> tuple:
+    """(algorithmic bytes of one step, bytes of its inputs: logits, x,
+    gate_up, expert_out)."""
+    ab = algorithmic_bytes(w)
+    inputs = 4 * w.T * w.E + 2 * w.T * w.H + 4 * w.S * w.I + 2 * w.S * w.H
+    return sum(ab.values()), inputs
+
+
+L2_BYTES = 129 * 10 ** 6
+
+
+def l2_note(w) -> str:
+    total, inputs = step_bytes(w)
+    if inputs > L2_BYTES:
+        return (f"no flush: steps run back to back and one step streams {total / 1e6:.0f} MB "
+                f"(inputs {inputs / 1e6:.0f} MB) through the 129 MB L2, so every input is evicted "
+                "between its uses")
+    return (f"no flush: a latency workload whose inputs ({inputs / 1e6:.1f} MB) stay in the 129 MB L2 "
+            "between steps")
+
+
 def config_dict(w):
     return {"workload": w.describe(), "T": w.T, "H": w.H, "E": w.E, "k": w.k, "renorm": w.renorm,
-            "I": w.I, "storage": "bf16 activations, fp32 logits/weights",
-            "l2": "no flush: steps run back to back and one step streams ~450 MB (inputs 252 MB) "
-                  "through the 129 MB L2, so every input is evicted between its uses",
+            "I": w.I, "storage": "bf16 activations, fp32 logits/weights", "l2": l2_note(w),
             "parallelism": "replicas (one independent batch per GPU)"}
 
 
 # ---------------------------------------------------------------------------
+
+def kernel_split(w, per_kernel, peak) -> dict:
+    """Mean event duration, algorithmic bytes, GB/s and fraction of peak of
+    each of the four calls."""
+    ab = algorithmic_bytes(w)
+    kern = {}
+    for name in KERNELS:
+        us = 1e3 * sum(per_kernel[name]) / len(per_kernel[name])
+        gbs = ab[name] / (us * 1e-6) / 1e9
+        kern[name] = {"us": round(us, 3), "algorithmic_bytes": ab[name], "GBps": round(gbs, 1),
+                      "frac": round(gbs / peak, 4)}
+    kern["sum_of_kernels_us"] = round(sum(kern[n]["us"] for n in KERNELS), 3)
+    return kern
+
+
+def time_alone(step, name, reps, dev):
+    """One of the step's calls launched `reps` times back to back on the
+    step's own buffers (after one untimed launch); mean microseconds per
+    launch. Only meaningful where the call's inputs exceed L2, so that every
+    launch reads them from HBM."""
+    torch = step.torch
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    fn = {"expand": lambda: step.lib.moe_expand(*step.expand_args, sp),
+          "swiglu": lambda: step.lib.moe_swiglu(*step.swiglu_args, sp),
+          "combine": lambda: step.lib.moe_combine(*step.combine_args, sp)}[name]
+    assert fn() == 0
+    torch.cuda.synchronize(dev)
+    torch.cuda._sleep(4_000_000)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        assert fn() == 0
+    b.record()
+    torch.cuda.synchronize(dev)
+    return 1e3 * a.elapsed_time(b) / reps
+
+
+def measure_side(w, dev, scratch, steps, peak, seed):
+    """A whole-path step on another workload: back-to-back device-resident
+    steps (value) and the per-kernel event split."""
+    from memory_bound_moe_gb300.workloads import generate
+    step = Step(w, generate(w, seed=seed), dev)
+    ms, _ = time_device_resident(step, steps, 20, dev, scratch)
+    ms = reduce_max(ms)
+    total, _ = step_bytes(w)
+    kern = kernel_split(w, time_per_kernel(step, min(steps, 500), dev, scratch), peak)
+    res = {"workload": w.describe(), "steps": steps, "ms_per_step": round(ms, 5),
+           "tokens_per_s": round(job_throughput(_world(), w.T, ms), 1),
+           "step_bytes": total, "path_GBps": round(total / (ms * 1e-3) / 1e9, 1),
+           "path_frac": round(total / (ms * 1e-3) / 1e9 / peak, 4), "l2": l2_note(w), "kernels": kern}
+    del step
+    return res
+
+
+def _world() -> int:
+    return int(os.environ.get("WORLD_SIZE", "1"))
+
 
 def main():
     args = parse_args()
@@ -726,7 +889,6 @@ def main():
     scratch = (torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev),
                torch.ones((L2_FLUSH_BYTES // 4,), dtype=torch.float32, device=dev))
 
-    clocks = ClockSampler(str(torch.cuda.get_device_properties(dev).uuid))
     remeasured = False
     for attempt in range(2):
         clocks = ClockSampler(str(torch.cuda.get_device_properties(dev).uuid))
@@ -739,26 +901,28 @@ def main():
 
     ms_step = reduce_max(ms_step_local)
     value = job_throughput(world, w.T, ms_step)
-    per_kernel = time_per_kernel(step, min(args.steps, 1000), dev, scratch)
+    per_kernel = time_per_kernel(step, min(max(args.steps, 200), 1000), dev, scratch)
 
     peak, peak_src = peak_hbm()
-    ab = algorithmic_bytes(w)
-    kern = {}
-    for name in KERNELS:
-        us = 1e3 * sum(per_kernel[name]) / len(per_kernel[name])
-        gbs = ab[name] / (us * 1e-6) / 1e9
-        kern[name] = {"us": round(us, 3), "algorithmic_bytes": ab[name], "GBps": round(gbs, 1),
-                      "frac": round(gbs / peak, 4)}
-    kern["sum_of_kernels_us"] = round(sum(kern[n]["us"] for n in KERNELS), 3)
+    kern = kernel_split(w, per_kernel, peak)
     dominant = max(KERNELS, key=lambda n: kern[n]["us"])
-    total_bytes = sum(ab.values())
+    total_bytes, input_bytes = step_bytes(w)
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": kern[dominant]["GBps"], "peak": peak,
                 "unit": "GB/s", "frac": kern[dominant]["frac"],
                 "traffic": traffic_from_profiles(dominant, w.name),
+                "algorithmic_bytes": kern[dominant]["algorithmic_bytes"],
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                 else "fallback 6.8 TB/s",
                 "path_GBps": round(total_bytes / (ms_step * 1e-3) / 1e9, 1),
                 "path_frac": round(total_bytes / (ms_step * 1e-3) / 1e9 / peak, 4)}
+    # the dominant kernel alone, back to back on the step's own buffers when
+    # its inputs exceed L2 (every launch then reads them from HBM)
+    if dominant != "route" and kern[dominant]["algorithmic_bytes"] > 2 * L2_BYTES:
+        us = time_alone(step, dominant, 50, dev)
+        gbs = kern[dominant]["algorithmic_bytes"] / (us * 1e-6) / 1e9
+        roofline["alone_us"] = round(us, 3)
+        roofline["alone_GBps"] = round(gbs, 1)
+        roofline["alone_frac"] = round(gbs / peak, 4)
 
     e2e = None
     if not args.no_e2e:
@@ -770,18 +934,19 @@ def main():
                "how": "pinned host inputs copied every step in 32 MB chunks over 4 copy streams into "
                       "double-buffered device sets; the C-ABI calls through the Python binding; "
                       "out copied back on a separate stream"}
+    launches = step.launches_per_step * args.steps
 
     more = args.workload == WORKLOAD and not args.no_extras
+    side = None
+    if more:
+        del step
+        torch.cuda.empty_cache()
+        side = {}
+        for name in SIDE_WORKLOADS:
+            side[name] = measure_side(WORKLOADS[name], dev, scratch, args.extra_reps or 2000, peak, rank)
+            torch.cuda.empty_cache()
     decode = decode_latency(dev, reps=args.extra_reps or 2000) if more else None
     extras = extras_measurement(dev, reps=args.extra_reps or 240) if more else None
-
-    # the dominant kernel measured alone (extras: back-to-back launches over
-    # rotating input/output sets), beside the in-step figure above, which
-    # also carries the previous kernel's write-backs
-    alone = (extras or {}).get(f"{dominant}_bf16")
-    if alone is not None:
-        roofline["alone_GBps"] = alone["GBps"]
-        roofline["alone_frac"] = alone["frac"]
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
@@ -793,7 +958,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config_dict(w),
             "roofline": roofline, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": step.launches_per_step * args.steps,
+            "gpu_launches": launches,
+            "workloads": side,
             "decode_latency": decode,
             "extras": extras,
             "clocks": clk, "remeasured": remeasured, "wall_s_timed_region": round(wall, 3),
