@@ -39,14 +39,15 @@
 namespace moe {
 namespace {
 
-template <int GS, int EPL, int NT, bool LOCAL>
+template <int GS, int EPL, int NT, bool LOCAL, int N>
 __global__ void __launch_bounds__(NT) route_rank_kernel(RouteArgs a) {
     constexpr int NW = NT / kWarp;
     extern __shared__ int32_t smem[];
     int32_t* s_cnt = smem;                         // [NW][nloc]
     int32_t* s_tot = s_cnt + (size_t)NW * a.nloc;  // [Ep]
-    const int t0 = blockIdx.x * a.tpc;
-    const int t1 = min(a.T, t0 + a.tpc);
+    // this block's tokens (64-bit products: b * tpc may pass 2^31 for huge T)
+    const int t0 = int(min(int64_t(a.T), int64_t(blockIdx.x) * a.tpc));
+    const int t1 = int(min(int64_t(a.T), int64_t(t0) + a.tpc));
     // Warm L2 with this block's logit rows before waiting for the kernel
     // that produced them (a prefetch carries no data into the kernel).
     if (a.vec4 && t1 > t0) {
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(NT) route_rank_kernel(RouteArgs a) {
     pdl_wait_and_release();
     zero_warp_counters(s_cnt, a.nloc);
     int re[kRegRounds], rr[kRegRounds];
-    topk_rank_range<GS, EPL, NT, LOCAL>(a, t0, t1, s_cnt, re, rr);
+    topk_rank_range<GS, EPL, NT, LOCAL, N>(a, t0, t1, s_cnt, re, rr);
     __syncthreads();
     scan_over_warps<NT>(s_cnt, s_tot, a.nloc);
     for (int e = a.nloc + threadIdx.x; e < a.Ep; e += NT) s_tot[e] = 0;
@@ -176,8 +177,8 @@ __global__ void __launch_bounds__(NT) route_place_kernel(RouteArgs a) {
 
     // This thread's first slot, read before the count matrix so that both
     // loads are in flight together.
-    const int s0 = b * a.tpc * a.k;
-    const int s1 = min(a.T, (b + 1) * a.tpc) * a.k;
+    const int s0 = int(min(int64_t(a.T), int64_t(b) * a.tpc)) * a.k;
+    const int s1 = int(min(int64_t(a.T), int64_t(b + 1) * a.tpc)) * a.k;
     const int sf = s0 + threadIdx.x;
     int ef = 0, rf = 0;
     if (sf < s1) {
@@ -277,6 +278,9 @@ __global__ void __launch_bounds__(NT) route_fused_kernel(RouteArgs a) {
 #ifndef MOE_ROUTE_GMAX
 #define MOE_ROUTE_GMAX 128
 #endif
+#ifndef MOE_ROUTE_PAIR
+#define MOE_ROUTE_PAIR 1
+#endif
 constexpr int kNtSplit = MOE_ROUTE_NT;
 constexpr int kNtFused = MOE_ROUTE_FUSED_NT;
 
@@ -294,12 +298,16 @@ cudaError_t launch_route_t(const RoutePlan& p, const RouteArgs& a, cudaStream_t 
         if ((err = allow_smem(kf, p.smem_topk)) != cudaSuccess) return err;
         return launch_pdl(kf, dim3(1), dim3(kNtFused), p.smem_topk, stream, a);
     }
-    auto k1 = route_rank_kernel<GS, EPL, kNtSplit, LOCAL>;
-    auto k2 = route_place_kernel<kNtSplit, LOCAL>;
+    // two tokens per step where a warp owns two or more (32-lane groups, at
+    // most 8 keys per lane: the pair's keys stay in registers)
+    constexpr bool kCanPair = MOE_ROUTE_PAIR && GS == 32 && EPL <= 8;
+    auto k1 = (kCanPair && p.tpw >= 2) ? route_rank_kernel<GS, EPL, kNtSplit, LOCAL, kCanPair ? 2 : 1>
+                                       : route_rank_kernel<GS, EPL, kNtSplit, LOCAL, 1>;
     if ((err = allow_smem(k1, p.smem_topk)) != cudaSuccess) return err;
-    if ((err = allow_smem(k2, p.smem_scatter)) != cudaSuccess) return err;
     if ((err = launch_pdl(k1, dim3(p.G), dim3(kNtSplit), p.smem_topk, stream, a)) != cudaSuccess)
         return err;
+    auto k2 = route_place_kernel<kNtSplit, LOCAL>;
+    if ((err = allow_smem(k2, p.smem_scatter)) != cudaSuccess) return err;
     return launch_pdl(k2, dim3(p.G), dim3(kNtSplit), p.smem_scatter, stream, a);
 }
 

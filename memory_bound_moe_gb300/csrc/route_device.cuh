@@ -107,13 +107,16 @@ __device__ __forceinline__ void load_keys(const RouteArgs& a, int t, bool valid,
         key[i] = (valid && e0 + i < a.E) ? order_key(__ldg(row + i)) : 0u;
 }
 
-// Top-k of one token by a group of GS lanes holding its keys in expert order
-// (the float is recovered exactly from its key). Pick j is the largest key
-// left and, among equal keys, the lowest expert. Each lane offers its best key
-// (the lowest of its experts among equal keys); the pick is the group maximum
-// of the offers, taken from the lowest lane offering it, which holds the
-// lowest such expert since lanes hold consecutive experts. One group maximum
-// and one ballot per pick.
+// Top-k of N tokens at once, each by the same group of GS lanes holding its
+// keys in expert order (the float is recovered exactly from its key). With
+// N > 1 the tokens' selections are independent dependency chains written as
+// one interleaved instruction stream, so each one's reduction latencies hide
+// behind the other's.
+// Pick j is the largest key left and, among equal keys, the lowest expert.
+// Each lane offers its best key (the lowest of its experts among equal keys);
+// the pick is the group maximum of the offers, taken from the lowest lane
+// offering it, which holds the lowest such expert since lanes hold
+// consecutive experts. One group maximum and one ballot per pick.
 //   EPL <= 8: a lane first sorts its keys in descending order by swapping
 //   neighbours only when the later key is strictly larger, so equal keys keep
 //   their expert order; its offer is then the head of the list, and the
@@ -121,110 +124,249 @@ __device__ __forceinline__ void load_keys(const RouteArgs& a, int t, bool valid,
 //   position is packed into one register, LB bits each.
 //   EPL > 8: a lane takes the arg-max of its keys every round and the owner
 //   zeroes the picked key.
-// Lane j < k keeps the j-th pick, writes it and its weight, and returns the
-// expert (-1 for lanes without a pick). Every lane of the warp must call
-// (valid may differ between groups of one warp; invalid groups compute on
-// empty keys and write nothing).
-template <int GS, int EPL>
-__device__ __forceinline__ int topk_select(const RouteArgs& a, int t, bool valid, int gl,
-                                           uint32_t (&key)[EPL]) {
+// Lane j < k keeps the j-th pick of every token, writes it and its weight,
+// and returns the expert in out[n] (-1 for lanes without a pick or invalid
+// tokens). Every lane of the warp must call (valid may differ between groups
+// of one warp and between the N tokens; invalid tokens compute on empty keys
+// and write nothing).
+template <int GS, int EPL, int N>
+__device__ __forceinline__ void topk_select_n(const RouteArgs& a, const int (&t)[N], const bool (&valid)[N],
+                                              int gl, uint32_t (&key)[N][EPL], int (&out)[N]) {
     constexpr bool kSorted = EPL <= 8;
     constexpr int LB = EPL <= 2 ? 1 : EPL <= 4 ? 2 : 3;
     constexpr uint32_t kIdxMask = (1u << LB) - 1u;
     const int lane = threadIdx.x % kWarp;
     const unsigned gmask = GS == 32 ? kFull : (((1u << GS) - 1u) << (lane & ~(GS - 1)));
 
-    uint32_t pidx = 0;   // sorted: expert index (within the lane) of position q at bits q*LB
-    if constexpr (kSorted) {
-        uint32_t ix[EPL];
+    uint32_t pidx[N];   // sorted: expert index (within the lane) of position q at bits q*LB
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) ix[i] = uint32_t(i);
+    for (int n = 0; n < N; ++n) pidx[n] = 0;
+    if constexpr (kSorted) {
+        uint32_t ix[N][EPL];
+#pragma unroll
+        for (int n = 0; n < N; ++n)
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) ix[n][i] = uint32_t(i);
 #pragma unroll
         for (int p = 0; p < EPL; ++p) {
 #pragma unroll
             for (int i = p & 1; i + 1 < EPL; i += 2) {
-                const bool sw = key[i + 1] > key[i];
-                const uint32_t k0 = sw ? key[i + 1] : key[i], k1 = sw ? key[i] : key[i + 1];
-                const uint32_t i0 = sw ? ix[i + 1] : ix[i], i1 = sw ? ix[i] : ix[i + 1];
-                key[i] = k0; key[i + 1] = k1; ix[i] = i0; ix[i + 1] = i1;
+#pragma unroll
+                for (int n = 0; n < N; ++n) {
+                    const bool sw = key[n][i + 1] > key[n][i];
+                    const uint32_t k0 = sw ? key[n][i + 1] : key[n][i], k1 = sw ? key[n][i] : key[n][i + 1];
+                    const uint32_t i0 = sw ? ix[n][i + 1] : ix[n][i], i1 = sw ? ix[n][i] : ix[n][i + 1];
+                    key[n][i] = k0; key[n][i + 1] = k1; ix[n][i] = i0; ix[n][i + 1] = i1;
+                }
             }
         }
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) pidx |= ix[i] << (i * LB);
+        for (int n = 0; n < N; ++n)
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) pidx[n] |= ix[n][i] << (i * LB);
     }
-    // this lane's offer: best key and its expert index within the lane
-    auto offer = [&](uint32_t& bk, int& bi) {
+    // this lane's offer for token n: best key and its expert index within the lane
+    uint32_t bk[N];
+    int bi[N];
+    auto offer = [&](int n) {
         if constexpr (kSorted) {
-            bk = key[0];
-            bi = int(pidx & kIdxMask);
+            bk[n] = key[n][0];
+            bi[n] = int(pidx[n] & kIdxMask);
         } else {
-            bk = key[0];
-            bi = 0;
+            bk[n] = key[n][0];
+            bi[n] = 0;
 #pragma unroll
             for (int i = 1; i < EPL; ++i)
-                if (key[i] > bk) { bk = key[i]; bi = i; }
+                if (key[n][i] > bk[n]) { bk[n] = key[n][i]; bi[n] = i; }
         }
     };
 
-    uint32_t bk;
-    int bi;
-    offer(bk, bi);
-    const uint32_t top = group_max<GS>(bk);   // the first pick's key
-    const float vmax = key_value(top);
+    uint32_t top[N];
+    float vmax[N], z[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) offer(n);
+#pragma unroll
+    for (int n = 0; n < N; ++n) top[n] = group_max<GS>(bk[n]);   // the first pick's key
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        vmax[n] = key_value(top[n]);
+        z[n] = 0.0f;
+    }
     // Softmax denominator over all E experts (only without renormalisation),
     // taken before the picks remove keys.
-    float z = 0.0f;
     if (!a.renorm) {
 #pragma unroll
-        for (int i = 0; i < EPL; ++i)
-            if (key[i] != 0u) z += expf(key_value(key[i]) - vmax);
-        z = group_sum<GS>(z);
+        for (int n = 0; n < N; ++n)
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (key[n][i] != 0u) z[n] += expf(key_value(key[n][i]) - vmax[n]);
+#pragma unroll
+        for (int n = 0; n < N; ++n) z[n] = group_sum<GS>(z[n]);
     }
 
-    uint32_t my_key = 0;
-    int my_id = 0;
+    uint32_t my_key[N];
+    int my_id[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) { my_key[n] = 0; my_id[n] = 0; }
 #pragma unroll
     for (int j = 0; j < kMaxTopk; ++j) {
         if (j >= a.k) break;
-        if (j > 0) offer(bk, bi);
-        const uint32_t gk = (j == 0) ? top : group_max<GS>(bk);
-        const unsigned bal = __ballot_sync(kFull, bk == gk) & gmask;
-        const int ol = __ffs(bal) - 1;   // owner: a lane of this group
-        const int id = __shfl_sync(kFull, gl * EPL + bi, ol);
-        const bool own = ol == lane;
-        if constexpr (kSorted) {
+        uint32_t gk[N];
+        unsigned bal[N];
+        int ol[N], id[N];
+        if (j > 0) {
 #pragma unroll
-            for (int i = 0; i + 1 < EPL; ++i) key[i] = own ? key[i + 1] : key[i];
-            key[EPL - 1] = own ? 0u : key[EPL - 1];
-            pidx = own ? pidx >> LB : pidx;
+            for (int n = 0; n < N; ++n) offer(n);
+#pragma unroll
+            for (int n = 0; n < N; ++n) gk[n] = group_max<GS>(bk[n]);
         } else {
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) key[i] = (own && i == bi) ? 0u : key[i];
+            for (int n = 0; n < N; ++n) gk[n] = top[n];
         }
-        if (gl == j) { my_key = gk; my_id = id; }
+#pragma unroll
+        for (int n = 0; n < N; ++n) bal[n] = __ballot_sync(kFull, bk[n] == gk[n]) & gmask;
+#pragma unroll
+        for (int n = 0; n < N; ++n) ol[n] = __ffs(bal[n]) - 1;   // owner: a lane of this group
+#pragma unroll
+        for (int n = 0; n < N; ++n) id[n] = __shfl_sync(kFull, gl * EPL + bi[n], ol[n]);
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            const bool own = ol[n] == lane;
+            if constexpr (kSorted) {
+#pragma unroll
+                for (int i = 0; i + 1 < EPL; ++i) key[n][i] = own ? key[n][i + 1] : key[n][i];
+                key[n][EPL - 1] = own ? 0u : key[n][EPL - 1];
+                pidx[n] = own ? pidx[n] >> LB : pidx[n];
+            } else {
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) key[n][i] = (own && i == bi[n]) ? 0u : key[n][i];
+            }
+            if (gl == j) { my_key[n] = gk[n]; my_id[n] = id[n]; }
+        }
     }
 
     // Weights in float32. The largest logit is the first pick.
     const bool mine = gl < a.k;
-    const float ej = mine ? expf(key_value(my_key) - vmax) : 0.0f;
-    float denom = z;                       // sum over all E experts
-    if (a.renorm) {                        // sum over the k picks (lanes 0..k-1)
-        denom = ej;
-        for (int o = 1; o < a.k; o <<= 1) denom += __shfl_xor_sync(kFull, denom, o);
+    float ej[N], denom[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        ej[n] = mine ? expf(key_value(my_key[n]) - vmax[n]) : 0.0f;
+        denom[n] = a.renorm ? ej[n] : z[n];   // sum over the k picks (lanes 0..k-1), or over all E
     }
-    if (valid && mine) {
-        if (a.write_out) {
-            a.topk_ids[(size_t)t * a.k + gl] = my_id;
-            a.topk_weights[(size_t)t * a.k + gl] = ej / denom;
+    if (a.renorm) {
+        for (int o = 1; o < a.k; o <<= 1) {
+#pragma unroll
+            for (int n = 0; n < N; ++n) denom[n] += __shfl_xor_sync(kFull, denom[n], o);
         }
-        return my_id;
     }
-    return -1;
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        out[n] = -1;
+        if (valid[n] && mine) {
+            if (a.write_out) {
+                a.topk_ids[(size_t)t[n] * a.k + gl] = my_id[n];
+                a.topk_weights[(size_t)t[n] * a.k + gl] = ej[n] / denom[n];
+            }
+            out[n] = my_id[n];
+        }
+    }
+}
+
+// One token per lane group (see topk_select_n).
+template <int GS, int EPL>
+__device__ __forceinline__ int topk_select(const RouteArgs& a, int t, bool valid, int gl, uint32_t (&key)[EPL]) {
+    const int tt[1] = {t};
+    const bool vv[1] = {valid};
+    uint32_t kk[1][EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) kk[0][i] = key[i];
+    int out[1];
+    topk_select_n<GS, EPL, 1>(a, tt, vv, gl, kk, out);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) key[i] = kk[0][i];
+    return out[0];
 }
 
 // Rounds whose (expert, rank) per lane stay in registers until the ranks are
 // finished; later rounds (only for very long token runs) go through inv_perm.
 constexpr int kRegRounds = 4;
+
+// The same for 32-lane groups (one token per round), two tokens per step:
+// a warp selects tokens w0 + r and w0 + r + 1 together (topk_select_n with
+// N = 2), keeping rounds r and r + 1 in re/rr. Ranks follow slot order, so
+// the first token's slots rank before the second's. A token's k experts are
+// distinct, so within one token every pick of an expert is its only one: the
+// rank of a pick is the warp's counter of its expert, read after the first
+// token's picks have been counted.
+template <int EPL, bool LOCAL>
+__device__ __forceinline__ void topk_rank_range_pairs(const RouteArgs& a, int t0, int t1, int32_t* s_cnt,
+                                                      int (&re)[kRegRounds], int (&rr)[kRegRounds]) {
+    constexpr int GS = 32;
+    static_assert(kRegRounds % 2 == 0, "rounds in pairs");
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    const int gl = lane;
+    int32_t* cnt = s_cnt + (size_t)warp * a.nloc;
+    const int w0 = t0 + warp * a.tpw;
+    const int w1 = min(t1, w0 + a.tpw);
+    auto counted = [&](int e) {
+        if constexpr (LOCAL) return (e < 0) ? -1 : (e >= a.e0 && e < a.e0 + a.nloc) ? e - a.e0 : -2;
+        else return e;
+    };
+    // ranks of the two tokens' picks (eA, eB counted indices), in slot order
+    auto rank2 = [&](int eA, int eB, int& rA, int& rB) {
+        rA = eA >= 0 ? cnt[eA] : 0;
+        __syncwarp();
+        if (eA >= 0) cnt[eA] = rA + 1;
+        __syncwarp();
+        rB = eB >= 0 ? cnt[eB] : 0;
+        __syncwarp();
+        if (eB >= 0) cnt[eB] = rB + 1;
+        __syncwarp();
+    };
+
+    uint32_t key[2][EPL], next[2][EPL];
+    load_keys<GS, EPL>(a, w0, w0 < w1, gl, key[0]);
+    load_keys<GS, EPL>(a, w0 + 1, w0 + 1 < w1, gl, key[1]);
+#pragma unroll
+    for (int r = 0; r < kRegRounds; r += 2) {
+        re[r] = re[r + 1] = -1;
+        rr[r] = rr[r + 1] = 0;
+        const int tA = w0 + r;
+        if (tA < w1) {
+            load_keys<GS, EPL>(a, tA + 2, tA + 2 < w1, gl, next[0]);
+            load_keys<GS, EPL>(a, tA + 3, tA + 3 < w1, gl, next[1]);
+            const int tt[2] = {tA, tA + 1};
+            const bool vv[2] = {true, tA + 1 < w1};
+            int e2[2];
+            topk_select_n<GS, EPL, 2>(a, tt, vv, gl, key, e2);
+            const int eA = counted(e2[0]), eB = counted(e2[1]);
+            int rA, rB;
+            rank2(eA, eB, rA, rB);
+            re[r] = eA; rr[r] = rA;
+            re[r + 1] = eB; rr[r + 1] = rB;
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) key[n][i] = next[n][i];
+        }
+    }
+    for (int tA = w0 + kRegRounds; tA < w1; tA += 2) {
+        const int tt[2] = {tA, tA + 1};
+        const bool vv[2] = {true, tA + 1 < w1};
+        int e2[2];
+        topk_select_n<GS, EPL, 2>(a, tt, vv, gl, key, e2);
+        load_keys<GS, EPL>(a, tA + 2, tA + 2 < w1, gl, key[0]);
+        load_keys<GS, EPL>(a, tA + 3, tA + 3 < w1, gl, key[1]);
+        const int eA = counted(e2[0]), eB = counted(e2[1]);
+        int rA, rB;
+        rank2(eA, eB, rA, rB);
+        if (eA >= 0) a.inv_perm[(size_t)tA * a.k + gl] = rA;
+        if (eA == -2) a.inv_perm[(size_t)tA * a.k + gl] = -1;
+        if (eB >= 0) a.inv_perm[(size_t)(tA + 1) * a.k + gl] = rB;
+        if (eB == -2) a.inv_perm[(size_t)(tA + 1) * a.k + gl] = -1;
+    }
+}
 
 // Top-k of the tokens [t0, t1) and the rank of every slot among this warp's
 // slots of the same expert; s_cnt is [NW][nloc] and counts each warp's picks
@@ -235,9 +377,13 @@ constexpr int kRegRounds = 4;
 // expert is not counted); the rank of later rounds is written to inv_perm[s]
 // (-1 for uncounted slots). The next round's logits are loaded before the
 // current round's selection. LOCAL counts only experts [e0, e0 + nloc).
-template <int GS, int EPL, int NT, bool LOCAL = false>
+template <int GS, int EPL, int NT, bool LOCAL = false, int N = 1>
 __device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int t1, int32_t* s_cnt,
                                                 int (&re)[kRegRounds], int (&rr)[kRegRounds]) {
+    if constexpr (N == 2) {
+        topk_rank_range_pairs<EPL, LOCAL>(a, t0, t1, s_cnt, re, rr);
+        return;
+    }
     constexpr int GPW = kWarp / GS;
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;

@@ -161,6 +161,11 @@ ROUTE_CASES = [
     (2048, 256, 8, False, "normal"), (5000, 5, 2, True, "ties"), (3000, 512, 16, True, "normal"),
     (4099, 1024, 16, True, "normal"), (20000, 128, 8, True, "normal"), (70000, 8, 2, True, "normal"),
     (129, 2, 2, True, "ties"), (300, 1, 1, True, "normal"),
+    # two tokens per warp step in the rank kernel: 256 and 160 experts (8 keys
+    # per lane), and odd token runs per warp (3 and 47 tokens) with rounds
+    # past the register-held ones
+    (8192, 256, 8, True, "normal"), (40001, 160, 6, False, "ties"), (6000, 100, 4, True, "normal"),
+    (94000, 64, 2, True, "ties"),
 ]
 
 
