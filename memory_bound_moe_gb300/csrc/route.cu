@@ -59,15 +59,17 @@ __global__ void __launch_bounds__(NT) route_rank_kernel(RouteArgs a) {
     }
     pdl_wait_and_release();
     zero_warp_counters(s_cnt, a.nloc);
-    int re[kRegRounds], rr[kRegRounds];
-    topk_rank_range<GS, EPL, NT, LOCAL, N>(a, t0, t1, s_cnt, re, rr);
+    // rounds held in registers: the wide blocks give every warp one token
+    constexpr int R = NT > 512 ? 1 : kRegRounds;
+    int re[R], rr[R];
+    topk_rank_range<GS, EPL, NT, LOCAL, N, R>(a, t0, t1, s_cnt, re, rr);
     __syncthreads();
     scan_over_warps<NT>(s_cnt, s_tot, a.nloc);
     for (int e = a.nloc + threadIdx.x; e < a.Ep; e += NT) s_tot[e] = 0;
     __syncthreads();
     int32_t* row = a.ws_counts + (size_t)blockIdx.x * a.Ep;
     for (int e = threadIdx.x; e < a.Ep; e += NT) row[e] = s_tot[e];
-    finish_ranks<GS, NT, false, LOCAL>(a, t0, t1, s_cnt, nullptr, re, rr);
+    finish_ranks<GS, NT, false, LOCAL, R>(a, t0, t1, s_cnt, nullptr, re, rr);
 }
 
 // The place kernel's split of the count matrix: column groups of 4 experts
@@ -272,6 +274,13 @@ __global__ void __launch_bounds__(NT) route_fused_kernel(RouteArgs a) {
 #ifndef MOE_ROUTE_NT
 #define MOE_ROUTE_NT 512
 #endif
+// Wide blocks of the two-kernel path: for 32-lane groups with 2 to 8 keys
+// per lane, when blocks of MOE_ROUTE_NT threads would give each warp two
+// tokens, blocks of this many give each warp one (every token of a block in
+// flight at once). 0 turns them off.
+#ifndef MOE_ROUTE_WIDE_NT
+#define MOE_ROUTE_WIDE_NT 1024
+#endif
 #ifndef MOE_ROUTE_FUSED_NT
 #define MOE_ROUTE_FUSED_NT 512
 #endif
@@ -283,11 +292,30 @@ __global__ void __launch_bounds__(NT) route_fused_kernel(RouteArgs a) {
 #endif
 constexpr int kNtSplit = MOE_ROUTE_NT;
 constexpr int kNtFused = MOE_ROUTE_FUSED_NT;
+constexpr int kNtWide = MOE_ROUTE_WIDE_NT;
+constexpr bool wide_eligible(int gs, int epl) { return kNtWide > kNtSplit && gs == 32 && epl >= 2 && epl <= 8; }
 
 template <typename K>
 cudaError_t allow_smem(K kernel, size_t bytes) {
     if (bytes <= 48 * 1024) return cudaSuccess;
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+}
+
+// The two-kernel path with blocks of NT threads.
+template <int GS, int EPL, bool LOCAL, int NT>
+cudaError_t launch_split(const RoutePlan& p, const RouteArgs& a, cudaStream_t stream) {
+    cudaError_t err;
+    // two tokens per step where a warp owns two or more (32-lane groups, at
+    // most 8 keys per lane: the pair's keys stay in registers; 512-thread
+    // blocks, whose register budget holds them)
+    constexpr bool kCanPair = MOE_ROUTE_PAIR && GS == 32 && EPL <= 8 && NT <= 512;
+    auto k1 = (kCanPair && p.tpw >= 2) ? route_rank_kernel<GS, EPL, NT, LOCAL, kCanPair ? 2 : 1>
+                                       : route_rank_kernel<GS, EPL, NT, LOCAL, 1>;
+    if ((err = allow_smem(k1, p.smem_topk)) != cudaSuccess) return err;
+    if ((err = launch_pdl(k1, dim3(p.G), dim3(NT), p.smem_topk, stream, a)) != cudaSuccess) return err;
+    auto k2 = route_place_kernel<NT, LOCAL>;
+    if ((err = allow_smem(k2, p.smem_scatter)) != cudaSuccess) return err;
+    return launch_pdl(k2, dim3(p.G), dim3(NT), p.smem_scatter, stream, a);
 }
 
 template <int GS, int EPL, bool LOCAL>
@@ -298,17 +326,10 @@ cudaError_t launch_route_t(const RoutePlan& p, const RouteArgs& a, cudaStream_t 
         if ((err = allow_smem(kf, p.smem_topk)) != cudaSuccess) return err;
         return launch_pdl(kf, dim3(1), dim3(kNtFused), p.smem_topk, stream, a);
     }
-    // two tokens per step where a warp owns two or more (32-lane groups, at
-    // most 8 keys per lane: the pair's keys stay in registers)
-    constexpr bool kCanPair = MOE_ROUTE_PAIR && GS == 32 && EPL <= 8;
-    auto k1 = (kCanPair && p.tpw >= 2) ? route_rank_kernel<GS, EPL, kNtSplit, LOCAL, kCanPair ? 2 : 1>
-                                       : route_rank_kernel<GS, EPL, kNtSplit, LOCAL, 1>;
-    if ((err = allow_smem(k1, p.smem_topk)) != cudaSuccess) return err;
-    if ((err = launch_pdl(k1, dim3(p.G), dim3(kNtSplit), p.smem_topk, stream, a)) != cudaSuccess)
-        return err;
-    auto k2 = route_place_kernel<kNtSplit, LOCAL>;
-    if ((err = allow_smem(k2, p.smem_scatter)) != cudaSuccess) return err;
-    return launch_pdl(k2, dim3(p.G), dim3(kNtSplit), p.smem_scatter, stream, a);
+    if constexpr (wide_eligible(GS, EPL)) {
+        if (p.nt == kNtWide) return launch_split<GS, EPL, LOCAL, (kNtWide > kNtSplit ? kNtWide : kNtSplit)>(p, a, stream);
+    }
+    return launch_split<GS, EPL, LOCAL, kNtSplit>(p, a, stream);
 }
 
 template <bool LOCAL>
@@ -350,17 +371,20 @@ RoutePlan plan_route(int64_t T, int E, int k, int nloc) {
         p.smem_topk = sizeof(int32_t) * (size_t(nw) * nloc + 2 * size_t(p.Ep) + 4 + 32);
         return p;
     }
-    const int nw = kNtSplit / kWarp;
-    p.nt = kNtSplit;
-    const int groups = nw * gpw;
     const int gmax = std::max(1, std::min(MOE_ROUTE_GMAX, 32768 / p.Ep));
-    const int64_t tpc = std::max<int64_t>(groups, (T + gmax - 1) / gmax);
+    const int64_t tpc_min = (T + gmax - 1) / gmax;   // tokens per block at the most blocks
+    // NT threads per block: at least one lane group per warp of tokens
+    p.nt = kNtSplit;
+    if (wide_eligible(p.gs, p.epl) && tpc_min > kNtSplit / kWarp && tpc_min <= kNtWide / kWarp) p.nt = kNtWide;
+    const int nw = p.nt / kWarp;
+    const int groups = nw * gpw;
+    const int64_t tpc = std::max<int64_t>(groups, tpc_min);
     p.tpc = int(tpc);
     p.tpw = int(((tpc + nw - 1) / nw + gpw - 1) / gpw * gpw);
     p.G = int((T + tpc - 1) / tpc);
     p.ws_bytes = sizeof(int32_t) * size_t(p.G) * size_t(p.Ep);
     p.smem_topk = sizeof(int32_t) * (size_t(nw) * nloc + p.Ep);
-    const PlaceSplit q = place_split(p.Ep, kNtSplit);
+    const PlaceSplit q = place_split(p.Ep, p.nt);
     p.smem_scatter = sizeof(int32_t) * (size_t(2) * q.Rp * p.Ep + 3 * size_t(p.Ep) + 4);
     return p;
 }

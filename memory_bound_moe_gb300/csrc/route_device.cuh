@@ -372,15 +372,16 @@ __device__ __forceinline__ void topk_rank_range_pairs(const RouteArgs& a, int t0
 // slots of the same expert; s_cnt is [NW][nloc] and counts each warp's picks
 // per counted expert. Warp w owns tokens [t0 + w*tpw, t0 + (w+1)*tpw); each
 // round takes GPW consecutive tokens, one per lane group, so lane order
-// within a round is slot order. The first kRegRounds rounds return each
+// within a round is slot order. The first R rounds return each
 // lane's counted expert and rank in re/rr (re: -1 no slot, -2 a slot whose
 // expert is not counted); the rank of later rounds is written to inv_perm[s]
 // (-1 for uncounted slots). The next round's logits are loaded before the
 // current round's selection. LOCAL counts only experts [e0, e0 + nloc).
-template <int GS, int EPL, int NT, bool LOCAL = false, int N = 1>
+template <int GS, int EPL, int NT, bool LOCAL = false, int N = 1, int R = kRegRounds>
 __device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int t1, int32_t* s_cnt,
-                                                int (&re)[kRegRounds], int (&rr)[kRegRounds]) {
+                                                int (&re)[R], int (&rr)[R]) {
     if constexpr (N == 2) {
+        static_assert(R == kRegRounds, "pairs keep kRegRounds rounds in registers");
         topk_rank_range_pairs<EPL, LOCAL>(a, t0, t1, s_cnt, re, rr);
         return;
     }
@@ -401,7 +402,7 @@ __device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int 
     uint32_t key[EPL], next[EPL];
     load_keys<GS, EPL>(a, w0 + grp, w0 + grp < w1, gl, key);
 #pragma unroll
-    for (int r = 0; r < kRegRounds; ++r) {
+    for (int r = 0; r < R; ++r) {
         re[r] = -1;
         rr[r] = 0;
         const int tb = w0 + r * GPW;
@@ -420,7 +421,7 @@ __device__ __forceinline__ void topk_rank_range(const RouteArgs& a, int t0, int 
             for (int i = 0; i < EPL; ++i) key[i] = next[i];
         }
     }
-    for (int tb = w0 + kRegRounds * GPW; tb < w1; tb += GPW) {
+    for (int tb = w0 + R * GPW; tb < w1; tb += GPW) {
         const int t = tb + grp;
         const int e = counted(topk_select<GS, EPL>(a, t, t < w1, gl, key));
         const int tn = tb + GPW + grp;
@@ -512,10 +513,10 @@ __device__ int block_exclusive_scan(const int32_t* in, int32_t* out, int n, int3
 // offset is added too and the result is final: it goes to perm/inv_perm when
 // a.write_out and, if s_inv is given, to s_inv[s] (shared memory). Slots of
 // uncounted experts (LOCAL) get inv_perm -1.
-template <int GS, int NT, bool PLACE, bool LOCAL = false>
+template <int GS, int NT, bool PLACE, bool LOCAL = false, int R = kRegRounds>
 __device__ __forceinline__ void finish_ranks(const RouteArgs& a, int t0, int t1, const int32_t* s_cnt,
-                                             const int32_t* s_off, const int (&re)[kRegRounds],
-                                             const int (&rr)[kRegRounds], int32_t* s_inv = nullptr) {
+                                             const int32_t* s_off, const int (&re)[R],
+                                             const int (&rr)[R], int32_t* s_inv = nullptr) {
     constexpr int GPW = kWarp / GS;
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
@@ -525,7 +526,7 @@ __device__ __forceinline__ void finish_ranks(const RouteArgs& a, int t0, int t1,
     const int w0 = t0 + warp * a.tpw;
     const int w1 = min(t1, w0 + a.tpw);
 #pragma unroll
-    for (int r = 0; r < kRegRounds; ++r) {
+    for (int r = 0; r < R; ++r) {
         const int s = (w0 + r * GPW + grp) * a.k + gl;
         if (re[r] >= 0) {
             int p = rr[r] + start[re[r]];
@@ -540,9 +541,9 @@ __device__ __forceinline__ void finish_ranks(const RouteArgs& a, int t0, int t1,
             if (PLACE && s_inv != nullptr) s_inv[s] = -1;
         }
     }
-    // slots of rounds past kRegRounds (the two-kernel path only, where
+    // slots of rounds past R (the two-kernel path only, where
     // write_out holds): the rank was kept in inv_perm
-    const int s_lo = (w0 + kRegRounds * GPW) * a.k;
+    const int s_lo = (w0 + R * GPW) * a.k;
     for (int s = s_lo + lane; s < w1 * a.k; s += kWarp) {
         int e = __ldcg(a.topk_ids + s);
         if constexpr (LOCAL) {

@@ -166,6 +166,9 @@ ROUTE_CASES = [
     # past the register-held ones
     (8192, 256, 8, True, "normal"), (40001, 160, 6, False, "ties"), (6000, 100, 4, True, "normal"),
     (94000, 64, 2, True, "ties"),
+    # 1024-thread rank blocks (one token per warp): a ragged last block, and
+    # 8 keys per lane with ties
+    (3000, 100, 6, True, "normal"), (4096, 256, 8, False, "ties"),
 ]
 
 
