@@ -78,6 +78,75 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // --------------------------------------------------------------------------
+// Pairs of floats in one 64-bit register, for the packed float32 arithmetic
+// of sm_100 and later (mul/add/fma .f32x2: two IEEE round-to-nearest-even
+// operations in one instruction, each bit-identical to the scalar one).
+// --------------------------------------------------------------------------
+
+struct F2 {
+    uint64_t v;
+};
+
+__device__ __forceinline__ F2 f2(float lo, float hi) {
+    F2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f2_split(F2 a, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+}
+
+__device__ __forceinline__ F2 mul2(F2 a, F2 b) {
+    F2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+
+__device__ __forceinline__ F2 add2(F2 a, F2 b) {
+    F2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+
+// The two float32 values of a bfloat16x2 word (low half first), as a pair.
+__device__ __forceinline__ F2 bf16x2_to_f2(uint32_t w) {
+    return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// --------------------------------------------------------------------------
+// SwiGLU of two elements in float32: silu(g) * u with silu(g) = g / (1 + e^-g),
+// e^-g taken as 2^(-g * log2 e) (ex2.approx) and the quotient as g times the
+// approximate reciprocal (rcp.approx), both flushing subnormals to zero (an
+// e^-g below 2^-126 adds nothing to 1; for g below about -87 the quotient is
+// under 2^-126 and comes out as a signed zero); products and the sum are IEEE
+// float32 operations done as pairs. Every kernel that stores or quantizes an
+// activation uses this one formulation, so they agree bit for bit.
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+constexpr float kNegLog2e = -1.44269504088896340736f;   // -log2(e)
+
+__device__ __forceinline__ F2 swiglu2(F2 g, F2 u) {
+    float t0, t1;
+    f2_split(mul2(g, f2(kNegLog2e, kNegLog2e)), t0, t1);
+    float d0, d1;
+    f2_split(add2(f2(ex2_approx(t0), ex2_approx(t1)), f2(1.0f, 1.0f)), d0, d1);
+    return mul2(mul2(g, f2(rcp_approx(d0), rcp_approx(d1))), u);
+}
+
+// --------------------------------------------------------------------------
 // Programmatic dependent launch (sm_90 and later; "CuTeDSL at Perplexity",
 // section "Grid synchronization", notes that it cuts launch overhead from
 // Hopper on). Kernels launched with launch_pdl() may be scheduled while the

@@ -21,7 +21,10 @@
 //    X + 127 (E8M0), code = E2M1(v * 2^-X).
 //  - NVFP4 (NVIDIA's format) with a float32 tensor scale g: scale byte
 //    E4M3(fl(fl(g * amax) / 6)) of value s, code = E2M1(fl(v * fl(g / s)))
-//    (0 when s = 0), every step one float32 rounding to nearest even.
+//    (0 when s = 0), every step one float32 rounding to nearest even. The
+//    division by 6 is a multiply and one corrected fused multiply-add
+//    (div6), and fl(g / s) comes from a per-block table of the 128
+//    possible scale values.
 //
 // Layout: codes [rows, n * bits / 8] bytes, row-major, two FP4 codes per byte
 // with element 2i in the low nibble; scales [rows, n / block] bytes,
@@ -94,8 +97,35 @@ struct QChunk {
     uint32_t scale;
 };
 
+// NVFP4: the multiplier fl(g / s) of every non-negative E4M3 scale byte
+// (value s; 0 for s = 0), one IEEE division each, computed once per block
+// before the dependency wait. Scale bytes of absolute maxima are at most
+// 0x7E (448, saturated).
+constexpr int kScaleTable = 128;
+
+__device__ __forceinline__ void fill_nvfp4_table(float* s_q, float g) {
+    for (int i = threadIdx.x; i < kScaleTable; i += blockDim.x) {
+        const float sv = e4m3_value(uint32_t(i));
+        s_q[i] = sv > 0.0f ? __fdiv_rn(g, sv) : 0.0f;
+    }
+}
+
+// fl(x / 6) for x >= 0 without a division: q0 = fl(x * fl(1/6)) corrected
+// by one fused multiply-add of its residual (Markstein's method). Checked
+// against the IEEE quotient for every finite float32: identical wherever the
+// quotient is a normal float; below 2^-126 both lie far under half the
+// smallest E4M3 step (2^-10), so the scale byte they round to is 0 either
+// way. Overflowed (infinite) x passes through.
+__device__ __forceinline__ float div6(float x) {
+    constexpr float kSixth = 1.0f / 6.0f;
+    const float q0 = __fmul_rn(x, kSixth);
+    const float r = __fmaf_rn(-q0, 6.0f, x);
+    return x < __int_as_float(0x7f800000) ? __fmaf_rn(r, kSixth, q0) : x;
+}
+
 template <int F, int EPT>
-__device__ __forceinline__ QChunk<F, EPT> quantize_chunk(const float (&v)[EPT], bool valid, float g) {
+__device__ __forceinline__ QChunk<F, EPT> quantize_chunk(const float (&v)[EPT], bool valid, float g,
+                                                         const float* s_q) {
     constexpr int kLanes = FmtInfo<F>::kBlock / EPT;
     float amax = 0.0f;
 #pragma unroll
@@ -104,21 +134,18 @@ __device__ __forceinline__ QChunk<F, EPT> quantize_chunk(const float (&v)[EPT], 
 #pragma unroll
     for (int o = 1; o < kLanes; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
     QChunk<F, EPT> c;
-    float p[EPT];   // the values the element conversion rounds
+    float m;   // the values' multiplier before the element conversion
     if constexpr (F == kNvfp4) {
-        const float t = __fdiv_rn(__fmul_rn(g, amax), 6.0f);
-        c.scale = pack_e4m3x2(t, 0.0f) & 0xffu;
-        const float sv = e4m3_value(c.scale);
-        const float q = sv > 0.0f ? __fdiv_rn(g, sv) : 0.0f;
-#pragma unroll
-        for (int i = 0; i < EPT; ++i) p[i] = __fmul_rn(v[i], q);
+        c.scale = pack_e4m3x2(div6(__fmul_rn(g, amax)), 0.0f) & 0xffu;
+        m = s_q[c.scale & (kScaleTable - 1)];
     } else {
         const int x = mx_exponent<F == kMxfp8 ? 8 : 2>(amax);
         c.scale = uint32_t(x + 127);
-        const float s = exp2_neg(min(x, 126));
-#pragma unroll
-        for (int i = 0; i < EPT; ++i) p[i] = v[i] * s;   // exact: a power of two
+        m = exp2_neg(min(x, 126));   // exact: a power of two
     }
+    float p[EPT];   // the values the element conversion rounds: fl(v * m), as pairs
+#pragma unroll
+    for (int i = 0; i < EPT; i += 2) f2_split(mul2(f2(v[i], v[i + 1]), f2(m, m)), p[i], p[i + 1]);
     if constexpr (F == kMxfp8) {
 #pragma unroll
         for (int q = 0; q < EPT / 4; ++q)
@@ -156,10 +183,6 @@ __device__ __forceinline__ void unpack(const Bits<2 * EPT>& b, float (&v)[EPT]) 
     }
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) {
-    return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
-
 // Byte offset of value column col of a row in the code buffer.
 template <int F>
 __device__ __forceinline__ uint64_t code_offset(uint64_t row, uint32_t n, uint32_t col) {
@@ -175,6 +198,11 @@ __global__ void __launch_bounds__(NT) swiglu_q_kernel(const uint8_t* __restrict_
                                                       DivU32 nv, uint32_t I, float g) {
     constexpr int VB = 2 * EPT;   // bytes of EPT bfloat16 inputs
     constexpr int kLanes = FmtInfo<F>::kBlock / EPT;
+    __shared__ float s_q[F == kNvfp4 ? kScaleTable : 1];
+    if constexpr (F == kNvfp4) {
+        fill_nvfp4_table(s_q, g);
+        __syncthreads();
+    }
     pdl_wait_and_release();
     const uint32_t stride = gridDim.x * NT;
     // the loop runs the same number of times on every lane of a warp (lanes
@@ -192,21 +220,20 @@ __global__ void __launch_bounds__(NT) swiglu_q_kernel(const uint8_t* __restrict_
             Bits<VB> gb, ub;
             ld_stream(gb, src);
             ld_stream(ub, src + 2ull * I);
-            float gf[EPT], uf[EPT];
-            unpack<EPT>(gb, gf);
-            unpack<EPT>(ub, uf);
 #pragma unroll
-            for (int i = 0; i < EPT; i += 2) {
+            for (int w = 0; w < EPT / 2; ++w) {
                 // the bfloat16 value moe_swiglu would store
-                const uint32_t b = pack_bf16x2(silu_mul(gf[i], uf[i]), silu_mul(gf[i + 1], uf[i + 1]));
-                a[i] = bf16_lo(b);
-                a[i + 1] = bf16_hi(b);
+                float lo, hi;
+                f2_split(swiglu2(bf16x2_to_f2(gb.w[w]), bf16x2_to_f2(ub.w[w])), lo, hi);
+                const uint32_t b = pack_bf16x2(lo, hi);
+                a[2 * w] = bf16_lo(b);
+                a[2 * w + 1] = bf16_hi(b);
             }
         } else {
 #pragma unroll
             for (int i = 0; i < EPT; ++i) a[i] = 0.0f;
         }
-        const QChunk<F, EPT> q = quantize_chunk<F, EPT>(a, valid, g);
+        const QChunk<F, EPT> q = quantize_chunk<F, EPT>(a, valid, g, s_q);
         if (valid) {
             store_words(codes + code_offset<F>(r, I, c * EPT), q.codes);
             if (c % kLanes == 0)
@@ -226,6 +253,11 @@ __global__ void __launch_bounds__(NT) expand_q_kernel(const uint8_t* __restrict_
                                                       uint32_t H, float g) {
     constexpr int VB = 2 * EPT;
     constexpr int kLanes = FmtInfo<F>::kBlock / EPT;
+    __shared__ float s_q[F == kNvfp4 ? kScaleTable : 1];
+    if constexpr (F == kNvfp4) {
+        fill_nvfp4_table(s_q, g);
+        __syncthreads();
+    }
     pdl_wait_and_release();
     const uint32_t stride = gridDim.x * NT;
     const uint32_t first = blockIdx.x * NT + (threadIdx.x & ~31u);
@@ -244,7 +276,7 @@ __global__ void __launch_bounds__(NT) expand_q_kernel(const uint8_t* __restrict_
 #pragma unroll
             for (int i = 0; i < EPT; ++i) a[i] = 0.0f;
         }
-        const QChunk<F, EPT> q = quantize_chunk<F, EPT>(a, valid, g);
+        const QChunk<F, EPT> q = quantize_chunk<F, EPT>(a, valid, g, s_q);
         if (valid) {
             const bool scale_lane = c % kLanes == 0;
             const int32_t* ip = inv_perm + uint64_t(t) * k;

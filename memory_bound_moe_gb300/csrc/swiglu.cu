@@ -10,7 +10,8 @@
 // busy for any I and no block shape depends on I.
 //
 //   act[r, i] = bf16_rn( silu(g) * u ), g = gate_up[r, i], u = gate_up[r, I + i],
-//   silu(g) = g / (1 + e^-g) in float32 (fast exp and reciprocal).
+//   silu(g) = g / (1 + e^-g) in float32 (swiglu2: approximate exp2 and
+//   reciprocal, the rest as IEEE float32 pair operations).
 #include "moe_device.cuh"
 #include "moe_launch.h"
 #include "rows_common.cuh"
@@ -18,16 +19,12 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ float silu_mul(float g, float u) {
-    return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
-
 template <int VB>
 __device__ __forceinline__ void swiglu_vec(const Bits<VB>& g, const Bits<VB>& u, Bits<VB>& o) {
 #pragma unroll
     for (int w = 0; w < VB / 4; ++w) {
-        const float lo = silu_mul(bf16_lo(g.w[w]), bf16_lo(u.w[w]));
-        const float hi = silu_mul(bf16_hi(g.w[w]), bf16_hi(u.w[w]));
+        float lo, hi;
+        f2_split(swiglu2(bf16x2_to_f2(g.w[w]), bf16x2_to_f2(u.w[w])), lo, hi);
         o.w[w] = pack_bf16x2(lo, hi);
     }
 }
