@@ -89,9 +89,12 @@ __global__ void __launch_bounds__(NT) combine_kernel(const uint8_t* __restrict__
 #ifndef MOE_COMBINE_NT
 #define MOE_COMBINE_NT 256
 #endif
-// k below this uses 32-byte vectors (k * 8 registers of loads in flight)
+// k below this uses 32-byte vectors (k * 8 registers of loads in flight).
+// Measured on GB300: 32-byte vectors win for k = 2 (prefill step 268.5 us
+// against 270.5 with 16-byte ones), 16-byte vectors for k = 4 (twice the
+// threads for the same bytes; skewed step 27.6 us against 29.2).
 #ifndef MOE_COMBINE_WIDE_BELOW_K
-#define MOE_COMBINE_WIDE_BELOW_K 8
+#define MOE_COMBINE_WIDE_BELOW_K 3
 #endif
 constexpr int kNt = MOE_COMBINE_NT;
 
@@ -133,8 +136,8 @@ cudaError_t launch_vb(const uint16_t* eo, int64_t rows, int64_t T, int H, int k,
 cudaError_t launch_combine(const uint16_t* expert_out, int64_t rows, int64_t T, int H, int k,
                            const float* topk_weights, const int32_t* inv_perm, uint16_t* out,
                            int num_sms, cudaStream_t stream) {
-    // 8 gathered rows of 32 bytes would hold 64 registers of loads per thread;
-    // large k keeps 16-byte vectors (still k loads in flight).
+    // 32-byte vectors only for k <= 2; larger k keeps 16-byte vectors (still
+    // k loads in flight, twice the threads).
     if (k < MOE_COMBINE_WIDE_BELOW_K && can_use_32b(uint64_t(H) * 2, {expert_out, out}))
         return launch_vb<32>(expert_out, rows, T, H, k, topk_weights, inv_perm, out, num_sms, stream);
     return launch_vb<16>(expert_out, rows, T, H, k, topk_weights, inv_perm, out, num_sms, stream);
