@@ -86,9 +86,6 @@ __global__ void __launch_bounds__(NT) combine_kernel(const uint8_t* __restrict__
     }
 }
 
-#ifndef MOE_COMBINE_NT
-#define MOE_COMBINE_NT 256
-#endif
 // k below this uses 32-byte vectors (k * 8 registers of loads in flight).
 // Measured on GB300: 32-byte vectors win for k = 2 (prefill step 268.5 us
 // against 270.5 with 16-byte ones), 16-byte vectors for k = 4 (twice the
@@ -96,22 +93,20 @@ __global__ void __launch_bounds__(NT) combine_kernel(const uint8_t* __restrict__
 #ifndef MOE_COMBINE_WIDE_BELOW_K
 #define MOE_COMBINE_WIDE_BELOW_K 3
 #endif
-constexpr int kNt = MOE_COMBINE_NT;
-
-template <int VB, int KT>
+template <int VB, int KT, int NT>
 cudaError_t launch_t(const uint16_t* eo, int64_t rows, int64_t T, int H, int k, const float* w,
                      const int32_t* inv_perm, uint16_t* out, int num_sms, cudaStream_t stream) {
-    auto kernel = combine_kernel<VB, KT, kNt>;
-    static const int occ = resident_blocks(kernel, kNt);
+    auto kernel = combine_kernel<VB, KT, NT>;
+    static const int occ = resident_blocks(kernel, NT);
     const uint32_t nv = uint32_t(uint64_t(H) * 2 / VB);
     const uint32_t S = uint32_t(rows);
     const int64_t tok_per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / nv));
     for (int64_t t0 = 0; t0 < T; t0 += tok_per_launch) {
         const int64_t nt = std::min(tok_per_launch, T - t0);
         const uint32_t total = uint32_t(nt * nv);
-        const int grid = grid_for(occ, total, uint64_t(kNt), num_sms);
+        const int grid = grid_for(occ, total, uint64_t(NT), num_sms);
         const cudaError_t err = launch_pdl(
-            kernel, dim3(grid), dim3(kNt), 0, stream, reinterpret_cast<const uint8_t*>(eo),
+            kernel, dim3(grid), dim3(NT), 0, stream, reinterpret_cast<const uint8_t*>(eo),
             reinterpret_cast<uint8_t*>(out + t0 * int64_t(H)), w + t0 * k, inv_perm + t0 * k, k, S,
             total, DivU32::make(nv), uint32_t(2 * int64_t(H)));
         if (err != cudaSuccess) return err;
@@ -119,15 +114,26 @@ cudaError_t launch_t(const uint16_t* eo, int64_t rows, int64_t T, int H, int k, 
     return cudaSuccess;
 }
 
+template <int VB, int KT>
+cudaError_t launch_k(const uint16_t* eo, int64_t rows, int64_t T, int H, int k, const float* w,
+                     const int32_t* inv_perm, uint16_t* out, int num_sms, cudaStream_t stream) {
+    switch (block_threads(uint64_t(T) * (uint64_t(H) * 2 / VB), num_sms)) {
+        case 256: return launch_t<VB, KT, 256>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        case 128: return launch_t<VB, KT, 128>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        case 64: return launch_t<VB, KT, 64>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        default: return launch_t<VB, KT, 32>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+    }
+}
+
 template <int VB>
 cudaError_t launch_vb(const uint16_t* eo, int64_t rows, int64_t T, int H, int k, const float* w,
                       const int32_t* inv_perm, uint16_t* out, int num_sms, cudaStream_t stream) {
     switch (k) {
-        case 1: return launch_t<VB, 1>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
-        case 2: return launch_t<VB, 2>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
-        case 4: return launch_t<VB, 4>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
-        case 8: return launch_t<VB, 8>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
-        default: return launch_t<VB, 0>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        case 1: return launch_k<VB, 1>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        case 2: return launch_k<VB, 2>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        case 4: return launch_k<VB, 4>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        case 8: return launch_k<VB, 8>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
+        default: return launch_k<VB, 0>(eo, rows, T, H, k, w, inv_perm, out, num_sms, stream);
     }
 }
 

@@ -73,10 +73,6 @@ __global__ void __launch_bounds__(NT) expand_kernel(const uint8_t* __restrict__ 
     }
 }
 
-#ifndef MOE_EXPAND_NT
-#define MOE_EXPAND_NT 256
-#endif
-constexpr int kNt = MOE_EXPAND_NT;
 // Blocks that prefetch x into L2 before waiting for the routing, used when x
 // takes at most a quarter of L2 (larger inputs would evict their own lines
 // before the copy reads them).
@@ -88,11 +84,11 @@ constexpr uint32_t kPrefetchBlocks = 64;
 #define MOE_EXPAND_U2_MIN_WARPS_PER_SM 32
 #endif
 
-template <int VB, int U>
-cudaError_t launch_vb(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm, int64_t rows,
+template <int VB, int U, int NT>
+cudaError_t launch_nt(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm, int64_t rows,
                       uint16_t* out, int num_sms, cudaStream_t stream) {
-    auto kernel = expand_kernel<VB, U, kNt>;
-    static const int occ = resident_blocks(kernel, kNt);
+    auto kernel = expand_kernel<VB, U, NT>;
+    static const int occ = resident_blocks(kernel, NT);
     const uint32_t nv = uint32_t(uint64_t(H) * 2 / VB);
     const uint32_t cpr = (nv + kWarp * U - 1) / (kWarp * U);
     const uint32_t row_bytes = uint32_t(2 * int64_t(H));
@@ -101,16 +97,29 @@ cudaError_t launch_vb(const uint16_t* x, int64_t T, int H, int k, const int32_t*
     for (int64_t t0 = 0; t0 < T; t0 += tok_per_launch) {
         const int64_t nt = std::min(tok_per_launch, T - t0);
         const uint32_t items = uint32_t(nt * cpr);
-        const int grid = grid_for(occ, items, uint64_t(kNt / kWarp), num_sms);
+        const int grid = grid_for(occ, items, uint64_t(NT / kWarp), num_sms);
         const uint64_t xb = uint64_t(nt) * row_bytes;
         const uint32_t pf = xb <= l2_bytes() / 4 ? std::min<uint32_t>(kPrefetchBlocks, uint32_t(grid)) : 0;
         const cudaError_t err = launch_pdl(
-            kernel, dim3(grid), dim3(kNt), 0, stream, reinterpret_cast<const uint8_t*>(x + t0 * int64_t(H)),
+            kernel, dim3(grid), dim3(NT), 0, stream, reinterpret_cast<const uint8_t*>(x + t0 * int64_t(H)),
             reinterpret_cast<uint8_t*>(out), inv_perm + t0 * k, k, uint32_t(rows), items, DivU32::make(cpr), nv,
             row_bytes, pf, xb);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
+}
+
+template <int VB, int U>
+cudaError_t launch_vb(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm, int64_t rows,
+                      uint16_t* out, int num_sms, cudaStream_t stream) {
+    const uint64_t nv = uint64_t(H) * 2 / VB;
+    const uint64_t lanes = uint64_t(T) * ((nv + kWarp * U - 1) / (kWarp * U)) * kWarp;
+    switch (block_threads(lanes, num_sms)) {
+        case 256: return launch_nt<VB, U, 256>(x, T, H, k, inv_perm, rows, out, num_sms, stream);
+        case 128: return launch_nt<VB, U, 128>(x, T, H, k, inv_perm, rows, out, num_sms, stream);
+        case 64: return launch_nt<VB, U, 64>(x, T, H, k, inv_perm, rows, out, num_sms, stream);
+        default: return launch_nt<VB, U, 32>(x, T, H, k, inv_perm, rows, out, num_sms, stream);
+    }
 }
 
 template <int VB>

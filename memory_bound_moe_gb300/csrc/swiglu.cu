@@ -64,34 +64,42 @@ __global__ void __launch_bounds__(NT) swiglu_kernel(const uint8_t* __restrict__ 
     }
 }
 
-#ifndef MOE_SWIGLU_NT
-#define MOE_SWIGLU_NT 256
-#endif
 #ifndef MOE_SWIGLU_UNROLL
 #define MOE_SWIGLU_UNROLL 1
 #endif
-constexpr int kNt = MOE_SWIGLU_NT;
 constexpr int kUnroll = MOE_SWIGLU_UNROLL;
 
-template <int VB>
-cudaError_t launch_vb(const uint16_t* gate_up, int64_t rows, int I, uint16_t* act, int num_sms,
+template <int VB, int NT>
+cudaError_t launch_nt(const uint16_t* gate_up, int64_t rows, int I, uint16_t* act, int num_sms,
                       cudaStream_t stream) {
-    auto kernel = swiglu_kernel<VB, kUnroll, kNt>;
-    static const int occ = resident_blocks(kernel, kNt);
+    auto kernel = swiglu_kernel<VB, kUnroll, NT>;
+    static const int occ = resident_blocks(kernel, NT);
     const uint32_t nv = uint32_t(uint64_t(I) * 2 / VB);
     const int64_t rows_per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / nv));
     for (int64_t r0 = 0; r0 < rows; r0 += rows_per_launch) {
         const int64_t nr = std::min(rows_per_launch, rows - r0);
         const uint32_t total = uint32_t(nr * nv);
-        const int grid = grid_for(occ, total, uint64_t(kNt) * kUnroll, num_sms);
+        const int grid = grid_for(occ, total, uint64_t(NT) * kUnroll, num_sms);
         const cudaError_t err = launch_pdl(
-            kernel, dim3(grid), dim3(kNt), 0, stream,
+            kernel, dim3(grid), dim3(NT), 0, stream,
             reinterpret_cast<const uint8_t*>(gate_up + r0 * 2 * int64_t(I)),
             reinterpret_cast<uint8_t*>(act + r0 * int64_t(I)), total, DivU32::make(nv),
             uint32_t(4 * int64_t(I)), uint32_t(2 * int64_t(I)));
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
+}
+
+template <int VB>
+cudaError_t launch_vb(const uint16_t* gate_up, int64_t rows, int I, uint16_t* act, int num_sms,
+                      cudaStream_t stream) {
+    const uint64_t threads = uint64_t(rows) * (uint64_t(I) * 2 / VB) / kUnroll;
+    switch (block_threads(threads, num_sms)) {
+        case 256: return launch_nt<VB, 256>(gate_up, rows, I, act, num_sms, stream);
+        case 128: return launch_nt<VB, 128>(gate_up, rows, I, act, num_sms, stream);
+        case 64: return launch_nt<VB, 64>(gate_up, rows, I, act, num_sms, stream);
+        default: return launch_nt<VB, 32>(gate_up, rows, I, act, num_sms, stream);
+    }
 }
 
 }  // namespace
