@@ -26,13 +26,14 @@ inline bool can_use_32b(uint64_t row_bytes, std::initializer_list<const void*> p
 // Measured on GB300 over the row kernels: the prefill step (16384 x 14336
 // SwiGLU outputs, ~12 items per thread at 4 waves) took 268.5 us at 4 waves,
 // 265.3 at 8 and 264.3 at 12 and 16; the smaller workloads and the quantized
-// kernels did not move, as their grids need fewer blocks than the cap.
+// kernels did not move, as their grids need fewer blocks than the cap. (QK
+// RMSNorm, 2 resident blocks per SM, passes its own cap.)
 #ifndef MOE_GRID_WAVES
 #define MOE_GRID_WAVES 16
 #endif
-inline int grid_for(int occ, uint64_t items, uint64_t per_block, int num_sms) {
+inline int grid_for(int occ, uint64_t items, uint64_t per_block, int num_sms, int waves = MOE_GRID_WAVES) {
     const uint64_t need = (items + per_block - 1) / per_block;
-    const uint64_t cap = uint64_t(num_sms) * uint64_t(std::max(occ, 1)) * MOE_GRID_WAVES;
+    const uint64_t cap = uint64_t(num_sms) * uint64_t(std::max(occ, 1)) * uint64_t(waves);
     return int(std::max<uint64_t>(1, std::min(need, cap)));
 }
 
