@@ -18,9 +18,10 @@
 //
 // The kernel is launched as a programmatic dependent of the routing. x does
 // not depend on the routing, so before waiting for it the first blocks issue
-// bulk L2 prefetches of x (when x is small next to L2): the reads overlap the
-// routing's last kernel, when HBM is nearly idle, and the copy then finds x in
-// L2 and spends HBM bandwidth on the stores.
+// bulk L2 prefetches of x (all of it when x is small next to L2, else its
+// first tokens): the reads overlap the routing's last kernel, when HBM is
+// nearly idle, and the copy then finds those rows in L2 and spends HBM
+// bandwidth on the stores.
 #include "moe_device.cuh"
 #include "moe_launch.h"
 #include "rows_common.cuh"
@@ -36,7 +37,8 @@ __global__ void __launch_bounds__(NT) expand_kernel(const uint8_t* __restrict__ 
                                                     uint32_t items, DivU32 cpr, uint32_t nv, uint32_t row_bytes,
                                                     uint32_t pf_blocks, uint64_t x_bytes) {
     // x does not depend on the routing this kernel waits for: the first
-    // pf_blocks blocks pull all of it into L2 while the routing still runs.
+    // pf_blocks blocks pull its first x_bytes into L2 while the routing still
+    // runs.
     if (blockIdx.x < pf_blocks) {
         constexpr uint32_t kPiece = 16384;
         const uint64_t slice = (x_bytes / pf_blocks + kPiece - 1) / kPiece * kPiece;
@@ -73,9 +75,9 @@ __global__ void __launch_bounds__(NT) expand_kernel(const uint8_t* __restrict__ 
     }
 }
 
-// Blocks that prefetch x into L2 before waiting for the routing, used when x
-// takes at most a quarter of L2 (larger inputs would evict their own lines
-// before the copy reads them).
+// Blocks that prefetch x into L2 before waiting for the routing. At most a
+// quarter of L2 is prefetched: more would evict its own first lines before
+// the copy reads them, and the routing's window is over by then anyway.
 constexpr uint32_t kPrefetchBlocks = 64;
 // Two vectors per lane and item once the items of U = 2 still give every SM
 // this many warps' worth (a few waves); fewer, smaller items otherwise, so
@@ -99,11 +101,14 @@ cudaError_t launch_nt(const uint16_t* x, int64_t T, int H, int k, const int32_t*
         const uint32_t items = uint32_t(nt * cpr);
         const int grid = grid_for(occ, items, uint64_t(NT / kWarp), num_sms);
         const uint64_t xb = uint64_t(nt) * row_bytes;
-        const uint32_t pf = xb <= l2_bytes() / 4 ? std::min<uint32_t>(kPrefetchBlocks, uint32_t(grid)) : 0;
+        // all of x when it takes at most a quarter of L2, else its first
+        // quarter-L2's worth: the first blocks copy the first tokens
+        const uint64_t pfb = std::min<uint64_t>(xb, l2_bytes() / 4 / 16384 * 16384);
+        const uint32_t pf = pfb > 0 ? std::min<uint32_t>(kPrefetchBlocks, uint32_t(grid)) : 0;
         const cudaError_t err = launch_pdl(
             kernel, dim3(grid), dim3(NT), 0, stream, reinterpret_cast<const uint8_t*>(x + t0 * int64_t(H)),
             reinterpret_cast<uint8_t*>(out), inv_perm + t0 * k, k, uint32_t(rows), items, DivU32::make(cpr), nv,
-            row_bytes, pf, xb);
+            row_bytes, pf, pfb);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
