@@ -103,6 +103,8 @@ struct QChunk {
 // 0x7E (448, saturated).
 constexpr int kScaleTable = 128;
 
+constexpr int kMaxTopK = 16;   // MOE_MAX_TOPK
+
 __device__ __forceinline__ void fill_nvfp4_table(float* s_q, float g) {
     for (int i = threadIdx.x; i < kScaleTable; i += blockDim.x) {
         const float sv = e4m3_value(uint32_t(i));
@@ -242,55 +244,127 @@ __global__ void __launch_bounds__(NT) swiglu_q_kernel(const uint8_t* __restrict_
     }
 }
 
-// Expand + block quantization: item v = t * nv + c covers x[t, c*EPT .. +EPT),
-// quantized once and stored to the token's k rows inv_perm[t*k + j] < rows.
-template <int F, int EPT, int NT>
+// Codes of one lane to one row: W words, one vector store (two for 64 bytes);
+// the address is aligned to min(4 W, 32) bytes.
+template <int W>
+__device__ __forceinline__ void store_code_words(uint8_t* p, const uint32_t (&w)[W]) {
+    if constexpr (W >= 8) {
+#pragma unroll
+        for (int h = 0; h < W / 8; ++h) {
+            Bits<32> b;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) b.w[i] = w[8 * h + i];
+            st_global(p + 32 * h, b);
+        }
+    } else {
+        store_words<W>(p, w);
+    }
+}
+
+// N scale bytes (packed in s, the first in the low byte) to an N-aligned
+// address.
+template <int N>
+__device__ __forceinline__ void store_scale_bytes(uint8_t* p, uint32_t s) {
+    if constexpr (N == 4) {
+        *reinterpret_cast<uint32_t*>(p) = s;
+    } else if constexpr (N == 2) {
+        *reinterpret_cast<uint16_t*>(p) = uint16_t(s);
+    } else {
+        *p = uint8_t(s);
+    }
+}
+
+// Expand + block quantization, in the row-chunk form of moe_expand. Work
+// item g = (token t, chunk c of 32 lane vectors); lane l of the warp that
+// takes it holds the V = U * VB / 2 consecutive values x[t, (32 c + l) V ...),
+// quantizes them once and stores their codes (one vector store) and scales
+// (one store) to each of the token's k rows inv_perm[t*k + j] < rows. The
+// k row indices are loaded once per item, index j by lane j, and broadcast
+// by shuffles. As in moe_expand, x does not depend on the routing this
+// kernel waits for: the first pf_blocks blocks prefetch its first x_bytes
+// into L2 before the wait.
+template <int F, int VB, int U, int NT>
 __global__ void __launch_bounds__(NT) expand_q_kernel(const uint8_t* __restrict__ x,
                                                       uint8_t* __restrict__ codes,
                                                       uint8_t* __restrict__ scales,
                                                       const int32_t* __restrict__ inv_perm, int k,
-                                                      uint32_t rows, uint32_t total, DivU32 nv,
-                                                      uint32_t H, float g) {
-    constexpr int VB = 2 * EPT;
-    constexpr int kLanes = FmtInfo<F>::kBlock / EPT;
+                                                      uint32_t rows, uint32_t items, DivU32 cpr, uint32_t H,
+                                                      float g, uint32_t pf_blocks, uint64_t x_bytes) {
+    constexpr int kBlock = FmtInfo<F>::kBlock;
+    constexpr int V = U * VB / 2;                 // values per lane
+    constexpr int EQ = V < kBlock ? V : kBlock;   // values per quantization call
+    constexpr int NQ = V / EQ;                    // calls (and scales) per lane
+    constexpr int kLanes = kBlock / EQ;           // lanes that share a scale
+    constexpr int QW = EQ * FmtInfo<F>::kBits / 32;
+    constexpr int VPL = VB / 2;                   // values per load
+    constexpr int NW = NT / kWarp;
+    if (blockIdx.x < pf_blocks) {
+        constexpr uint32_t kPiece = 16384;
+        const uint64_t slice = (x_bytes / pf_blocks + kPiece - 1) / kPiece * kPiece;
+        const uint64_t lo = uint64_t(blockIdx.x) * slice;
+        const uint64_t hi = min(x_bytes, lo + slice);
+        for (uint64_t off = lo + uint64_t(threadIdx.x) * kPiece; off < hi; off += uint64_t(NT) * kPiece)
+            prefetch_l2(x + off, uint32_t(min(uint64_t(kPiece), hi - off)));
+    }
     __shared__ float s_q[F == kNvfp4 ? kScaleTable : 1];
     if constexpr (F == kNvfp4) {
         fill_nvfp4_table(s_q, g);
         __syncthreads();
     }
     pdl_wait_and_release();
-    const uint32_t stride = gridDim.x * NT;
-    const uint32_t first = blockIdx.x * NT + (threadIdx.x & ~31u);
-    for (uint32_t wbase = first; wbase < total; wbase += stride) {
-        const uint32_t v = wbase + (threadIdx.x & 31u);
-        const bool valid = v < total;
-        uint32_t t = 0, c = 0;
-        float a[EPT];
+    const int lane = threadIdx.x % kWarp;
+    const uint32_t W = gridDim.x * NW;
+    const uint32_t sp = H / kBlock;   // scales per row
+    for (uint32_t gi = blockIdx.x * NW + threadIdx.x / kWarp; gi < items; gi += W) {
+        const uint32_t t = cpr.div(gi);
+        const uint32_t col = ((gi - t * cpr.d) * kWarp + lane) * V;
+        const bool valid = col < H;   // the row's last chunk may be partly outside it
+        const uint32_t pl = lane < k ? uint32_t(__ldg(inv_perm + uint64_t(t) * k + lane)) : 0u;
+        Bits<VB> b[U];
         if (valid) {
-            t = nv.div(v);
-            c = v - t * nv.d;
-            Bits<VB> b;
-            ld_stream(b, x + uint64_t(t) * (2ull * H) + uint64_t(c) * VB);
-            unpack<EPT>(b, a);
+#pragma unroll
+            for (int u = 0; u < U; ++u) ld_stream(b[u], x + (uint64_t(t) * H + col) * 2 + u * VB);
         } else {
 #pragma unroll
-            for (int i = 0; i < EPT; ++i) a[i] = 0.0f;
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int i = 0; i < VB / 4; ++i) b[u].w[i] = 0u;
         }
-        const QChunk<F, EPT> q = quantize_chunk<F, EPT>(a, valid, g, s_q);
-        if (valid) {
-            const bool scale_lane = c % kLanes == 0;
-            const int32_t* ip = inv_perm + uint64_t(t) * k;
-            for (int j = 0; j < k; ++j) {
-                const uint32_t p = uint32_t(__ldg(ip + j));
-                if (p >= rows) continue;
-                store_words(codes + code_offset<F>(p, H, c * EPT), q.codes);
-                if (scale_lane) scales[uint64_t(p) * (H / FmtInfo<F>::kBlock) + c / kLanes] = uint8_t(q.scale);
+        uint32_t cw[NQ * QW];
+        uint32_t sc = 0;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            float a[EQ];
+#pragma unroll
+            for (int e = 0; e < EQ; e += 2) {
+                const int i = q * EQ + e;
+                const uint32_t w = b[i / VPL].w[(i % VPL) / 2];
+                a[e] = bf16_lo(w);
+                a[e + 1] = bf16_hi(w);
+            }
+            const QChunk<F, EQ> qc = quantize_chunk<F, EQ>(a, valid, g, s_q);
+#pragma unroll
+            for (int w = 0; w < QW; ++w) cw[q * QW + w] = qc.codes[w];
+            sc |= (qc.scale & 0xffu) << (8 * q);
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j >= k) break;
+            const uint32_t p = uint32_t(__shfl_sync(kFull, pl, j));
+            if (!valid || p >= rows) continue;   // outside the row, or a slot without a row here
+            store_code_words(codes + code_offset<F>(p, H, col), cw);
+            uint8_t* sdst = scales + uint64_t(p) * sp + col / kBlock;
+            if constexpr (kLanes == 1) {
+                store_scale_bytes<NQ>(sdst, sc);
+            } else if (lane % kLanes == 0) {
+                *sdst = uint8_t(sc);
             }
         }
     }
 }
 
 constexpr int kNt = 256;
+constexpr uint32_t kPrefetchBlocks = 64;   // blocks that prefetch x in the quantized expand
 
 template <int F, int EPT>
 cudaError_t launch_swiglu_q(const uint16_t* gate_up, int64_t rows, int I, uint8_t* codes,
@@ -313,24 +387,66 @@ cudaError_t launch_swiglu_q(const uint16_t* gate_up, int64_t rows, int I, uint8_
     return cudaSuccess;
 }
 
-template <int F, int EPT>
+template <int F, int VB, int U, int NT>
 cudaError_t launch_expand_q(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm,
                             int64_t rows, uint8_t* codes, uint8_t* scales, float g, int num_sms,
                             cudaStream_t stream) {
-    auto kernel = expand_q_kernel<F, EPT, kNt>;
-    static const int occ = resident_blocks(kernel, kNt);
-    const uint32_t nv = uint32_t(H / EPT);
-    const int64_t per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / nv));
-    for (int64_t t0 = 0; t0 < T; t0 += per_launch) {
-        const int64_t nt = std::min(per_launch, T - t0);
-        const uint32_t total = uint32_t(nt * nv);
-        const int grid = grid_for(occ, total, uint64_t(kNt), num_sms);
+    auto kernel = expand_q_kernel<F, VB, U, NT>;
+    static const int occ = resident_blocks(kernel, NT);
+    constexpr uint32_t V = U * VB / 2;
+    const uint32_t cpr = (uint32_t(H) + kWarp * V - 1) / (kWarp * V);
+    // lanes of a launch (items * 32) stay below the per-launch item limit
+    const int64_t tok_per_launch = std::max<int64_t>(1, int64_t(kMaxItemsPerLaunch / (uint64_t(cpr) * kWarp)));
+    for (int64_t t0 = 0; t0 < T; t0 += tok_per_launch) {
+        const int64_t nt = std::min(tok_per_launch, T - t0);
+        const uint32_t items = uint32_t(nt * cpr);
+        const int grid = grid_for(occ, items, uint64_t(NT / kWarp), num_sms);
+        // all of x when it takes at most a quarter of L2, else its first
+        // quarter-L2's worth (the rows the first blocks quantize)
+        const uint64_t xb = uint64_t(nt) * 2 * uint64_t(H);
+        const uint64_t pfb = std::min<uint64_t>(xb, l2_bytes() / 4 / 16384 * 16384);
+        const uint32_t pf = pfb > 0 ? std::min<uint32_t>(kPrefetchBlocks, uint32_t(grid)) : 0;
         const cudaError_t err = launch_pdl(
-            kernel, dim3(grid), dim3(kNt), 0, stream, reinterpret_cast<const uint8_t*>(x + t0 * int64_t(H)),
-            codes, scales, inv_perm + t0 * k, k, uint32_t(rows), total, DivU32::make(nv), uint32_t(H), g);
+            kernel, dim3(grid), dim3(NT), 0, stream, reinterpret_cast<const uint8_t*>(x + t0 * int64_t(H)),
+            codes, scales, inv_perm + t0 * k, k, uint32_t(rows), items, DivU32::make(cpr), uint32_t(H), g, pf,
+            pfb);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
+}
+
+template <int F, int VB, int U>
+cudaError_t expand_q_u(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm, int64_t rows,
+                       uint8_t* codes, uint8_t* scales, float g, int num_sms, cudaStream_t stream) {
+    constexpr uint64_t V = U * VB / 2;
+    const uint64_t lanes = uint64_t(T) * ((uint64_t(H) + kWarp * V - 1) / (kWarp * V)) * kWarp;
+    switch (block_threads(lanes, num_sms)) {
+        case 256: return launch_expand_q<F, VB, U, 256>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream);
+        case 128: return launch_expand_q<F, VB, U, 128>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream);
+        case 64: return launch_expand_q<F, VB, U, 64>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream);
+        default: return launch_expand_q<F, VB, U, 32>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream);
+    }
+}
+
+// Two loads per lane once the items of that width still give every SM
+// this many warps' worth; fewer, smaller items otherwise, so that small
+// batches spread over all SMs.
+#ifndef MOE_EXPAND_Q_MIN_WARPS_PER_SM
+#define MOE_EXPAND_Q_MIN_WARPS_PER_SM 32
+#endif
+
+// Whether U loads of VB bytes per lane fit: whole lane vectors in a row, the
+// codes' and scales' vector stores aligned, and enough items for every SM.
+template <int F, int VB>
+bool expand_q_fits(int U, int64_t T, int H, const uint8_t* codes, const uint8_t* scales, int num_sms) {
+    const uint64_t V = uint64_t(U) * VB / 2;
+    if (uint64_t(H) % V != 0) return false;
+    const uint64_t code_bytes = V * FmtInfo<F>::kBits / 8;
+    if (reinterpret_cast<uintptr_t>(codes) % std::min<uint64_t>(code_bytes, 32) != 0) return false;
+    if (V >= uint64_t(FmtInfo<F>::kBlock) && reinterpret_cast<uintptr_t>(scales) % (V / FmtInfo<F>::kBlock) != 0)
+        return false;
+    const uint64_t items = uint64_t(T) * ((uint64_t(H) + kWarp * V - 1) / (kWarp * V));
+    return items >= uint64_t(num_sms) * MOE_EXPAND_Q_MIN_WARPS_PER_SM;
 }
 
 // 16 values per thread when the bfloat16 input rows allow 32-byte loads and
@@ -344,13 +460,20 @@ cudaError_t swiglu_q(const uint16_t* gate_up, int64_t rows, int I, uint8_t* code
     return launch_swiglu_q<F, 8>(gate_up, rows, I, codes, scales, g, num_sms, stream);
 }
 
+// 32-byte loads when the bfloat16 input rows allow them, else 16-byte ones;
+// then two of them per lane where that fits, else one. (Four per lane left
+// too few warps on mid-sized batches: 11.1 against 9.6 us for NVFP4 at
+// 4096 x 2048, top-8.)
 template <int F>
 cudaError_t expand_q(const uint16_t* x, int64_t T, int H, int k, const int32_t* inv_perm, int64_t rows,
                      uint8_t* codes, uint8_t* scales, float g, int num_sms, cudaStream_t stream) {
-    constexpr uint32_t kStore16 = 16 * FmtInfo<F>::kBits / 8;
-    if (can_use_32b(uint64_t(H) * 2, {x}) && reinterpret_cast<uintptr_t>(codes) % kStore16 == 0)
-        return launch_expand_q<F, 16>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream);
-    return launch_expand_q<F, 8>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream);
+    constexpr uint32_t kStore16 = 16 * FmtInfo<F>::kBits / 8;   // code bytes of 16 values
+    if (can_use_32b(uint64_t(H) * 2, {x}) && reinterpret_cast<uintptr_t>(codes) % kStore16 == 0) {
+        if (expand_q_fits<F, 32>(2, T, H, codes, scales, num_sms))
+            return expand_q_u<F, 32, 2>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream);
+        return expand_q_u<F, 32, 1>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream);
+    }
+    return expand_q_u<F, 16, 1>(x, T, H, k, inv_perm, rows, codes, scales, g, num_sms, stream);
 }
 
 }  // namespace
