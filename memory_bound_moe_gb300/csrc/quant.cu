@@ -175,16 +175,6 @@ __device__ __forceinline__ void store_words(uint8_t* p, const uint32_t (&w)[W]) 
     }
 }
 
-// bfloat16 bits -> the float values, EPT of them.
-template <int EPT>
-__device__ __forceinline__ void unpack(const Bits<2 * EPT>& b, float (&v)[EPT]) {
-#pragma unroll
-    for (int q = 0; q < EPT / 2; ++q) {
-        v[2 * q] = bf16_lo(b.w[q]);
-        v[2 * q + 1] = bf16_hi(b.w[q]);
-    }
-}
-
 // Byte offset of value column col of a row in the code buffer.
 template <int F>
 __device__ __forceinline__ uint64_t code_offset(uint64_t row, uint32_t n, uint32_t col) {
@@ -244,8 +234,8 @@ __global__ void __launch_bounds__(NT) swiglu_q_kernel(const uint8_t* __restrict_
     }
 }
 
-// Codes of one lane to one row: W words, one vector store (two for 64 bytes);
-// the address is aligned to min(4 W, 32) bytes.
+// Codes of one lane to one row: W words (at most 16), one vector store (two
+// for 64 bytes); the address is aligned to min(4 W, 32) bytes.
 template <int W>
 __device__ __forceinline__ void store_code_words(uint8_t* p, const uint32_t (&w)[W]) {
     if constexpr (W >= 8) {
